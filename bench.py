@@ -1,0 +1,289 @@
+"""Benchmark of the NVFP4 quantizer hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one tensor: nvfp4_amax (tensor
+amax per copy) then nvfp4_quantize (scale, round, pack; rowwise + transposed
+columnwise outputs).  The default workload is the recipe's activation tensor,
+8192 x 5120 bf16 with outlier channels, 4/6 with MAE selection, both copies.
+
+Metric: NVFP4 quantize GB/s = (bf16 bytes read + code bytes + scale bytes
+written) per step / step time.  L2 is flushed (a 512 MiB write) before every
+timed step.  The roofline entry is for the dominant kernel (quantize), timed
+with CUDA events on its own stream inside the timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the path needs
+no exchange for independent tensors) and rank 0 prints the JSON line with the
+max step time over ranks.  --impl reference times the CPU oracle on the host
+cores instead (a bounded row sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "NVFP4 quantize GB/s (bf16 in + fp4/scales out), % of GB300 HBM peak"
+UNIT = "GB/s"
+
+
+def algorithmic_bytes(M: int, N: int, flags: int) -> int:
+    """bf16 read + per copy (codes N*M/2 + scales N*M/16)."""
+    copies = (1 if flags & 1 else 0) + (1 if flags & 2 else 0)
+    return 2 * M * N + copies * (M * N // 2 + M * N // 16)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=5)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_bit_block_gb300 as nv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    nv.build() if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    nv.lib()
+    flags, sel = synthetic.workload_flags(args.workload)
+    bits = synthetic.workload(args.workload)
+    M, N = bits.shape
+    x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x = x_host.to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    amax = torch.empty(2, dtype=torch.float32, device=dev)
+    out = nv.nvfp4_quantize(x, nv.nvfp4_amax(x, flags, synthetic.RHT_SEED), flags, sel)  # allocate outputs
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        nv.nvfp4_amax(x, flags, synthetic.RHT_SEED, out=amax, stream=stream)
+        nv.nvfp4_quantize(x, amax, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, 0, out=out,
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.fill_(k & 0xFF)          # evict X from L2 before the step
+                ev[k][0].record(stream)
+                nv.nvfp4_amax(x, flags, synthetic.RHT_SEED, out=amax, stream=stream)
+                ev[k][1].record(stream)
+                nv.nvfp4_quantize(x, amax, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, 0, out=out,
+                                  stream=stream)
+                ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    amax_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    quant_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    status = int(out.status.item())
+    assert status == 0, f"quantize reported status {status}"
+
+    # end to end through the public API: pinned host x -> device -> amax ->
+    # quantize -> outputs back to pinned host buffers, every step
+    host_out = [torch.empty(t_.shape, dtype=t_.dtype, pin_memory=True)
+                for t_ in (out.q_row, out.s_row, out.q_col, out.s_col, out.alpha) if t_ is not None]
+    dev_out = [t_ for t_ in (out.q_row, out.s_row, out.q_col, out.s_col, out.alpha) if t_ is not None]
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for k in range(2 + e2e_steps):
+            if k == 2:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            x.copy_(x_host, non_blocking=True)
+            step()
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    d2h = sum(t_.numel() * t_.element_size() for t_ in dev_out)
+
+    nbytes = algorithmic_bytes(M, N, flags)
+    value = nbytes * args.steps / (total_ms * 1e-3) / 1e9 * world
+    peak, peak_kind = measured_peaks()
+    quant_avg_ms = statistics.mean(quant_ms)
+    achieved = nbytes / (quant_avg_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->nvfp4 (fp32 arithmetic)",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "flags": flags, "selection": sel,
+                   "elements": M * N, "bytes_per_step": nbytes,
+                   "l2": "512 MiB flush write before every timed step",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "kernels_ms": {"amax": round(statistics.mean(amax_ms), 5), "quantize": round(quant_avg_ms, 5)},
+        "elements_per_s": round(M * N * args.steps * world / (total_ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "quantize"},
+        "step_frac_of_peak": round(value / world / peak, 4),
+        "e2e": {"value": round(nbytes / e2e_s / 1e9 * world, 1), "unit": UNIT,
+                "h2d_bytes_per_step": 2 * M * N, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    return res
+
+
+def run_oracle_sample(args, max_seconds: float = 20.0):
+    """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle
+
+    flags, sel = synthetic.workload_flags(args.workload)
+    bits = synthetic.workload(args.workload)
+    M, N = bits.shape
+    t0 = time.perf_counter()
+    st, am = oracle.amax(bits, flags, synthetic.RHT_SEED)
+    t_amax = time.perf_counter() - t0
+    rows = 16
+    outs = oracle.output_buffers(M, N, flags)
+    elapsed = 0.0
+    done = 0
+    while elapsed < max_seconds / 2 and done < M:
+        n = min(rows, M - done)
+        t0 = time.perf_counter()
+        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
+                        row0=done, row1=done + n, outs=outs)
+        elapsed += time.perf_counter() - t0
+        done += n
+        rows = min(rows * 2, 1024)
+    frac = done / M
+    t_step = t_amax + elapsed / frac           # full-tensor estimate: amax + scaled quantize
+    nbytes = algorithmic_bytes(M, N, flags)
+    return {"value": round(nbytes / t_step / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"amax over the full {M}x{N} tensor ({t_amax:.2f} s) + quantize of the first "
+                      f"{done} rows ({elapsed:.2f} s), scaled to the full tensor"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="act_46mae_8192x5120", choices=list(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = []
+        cb = None
+        for _ in range(args.warmup + args.steps):
+            cb = run_oracle_sample(args, max_seconds=4.0)
+            per_step.append(cb["value"])
+        v = statistics.mean(per_step[args.warmup:]) if args.steps else per_step[-1]
+        flags, sel = synthetic.workload_flags(args.workload)
+        _, M, N = synthetic.WORKLOADS[args.workload][:3]
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": args.workload, "M": M, "N": N, "flags": flags, "selection": sel},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cb["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_oracle_sample(args)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -48,6 +48,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -98,7 +104,7 @@ typedef enum {
  *             gives NaN, an Inf input Inf.  Overwritten, not accumulated.
  * Returns NVFP4_OK or a host-side error (nothing enqueued then).
  */
-int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, uint32_t flags,
+NVFP4_API int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, uint32_t flags,
                uint64_t rht_seed, float* amax_dev, void* stream);
 
 /*
@@ -135,7 +141,7 @@ int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, uint32_t fla
  * With 2D, the tile scale is repeated in the 1x16 scale layouts (16 times in
  * s_row, 16 times in s_col) and C's codes are exactly the transpose of R's.
  */
-int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const float* amax_dev,
+NVFP4_API int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const float* amax_dev,
                    uint32_t flags, int sel, uint64_t sr_seed, uint64_t rht_seed,
                    uint64_t counter_offset, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                    uint8_t* s_col, float* alpha_dev, int* status_dev, void* stream);
@@ -151,11 +157,11 @@ int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const fl
  *              even (out_is_bf16 = 1); 16-byte aligned
  * cols % 16 == 0.  With an RHT copy the result is in the transformed basis.
  */
-int nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, const float* alpha_dev,
+NVFP4_API int nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, const float* alpha_dev,
                      int64_t rows, int64_t cols, int out_is_bf16, void* out_dev, void* stream);
 
 /* Human-readable name of a status value (static string). */
-const char* nvfp4_strerror(int status);
+NVFP4_API const char* nvfp4_strerror(int status);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,249 @@
+// nvfp4_device.cuh -- device building blocks of the NVFP4 quantizer (sm_103a).
+//
+// Every floating-point step of the quantizer's contract is written with an
+// explicit round-to-nearest intrinsic (__fmul_rn, __fadd_rn, __fdiv_rn,
+// __frcp_rn, __fmaf_rn) so that the compiler can neither fuse nor reorder it;
+// the library is also built with -fmad=false.  The E2M1 and E4M3 conversions
+// use the Blackwell cvt instructions (the "cvt family" that the 4/6 page's
+// Implementation details name), written here as inline PTX.
+//
+// Sources: "Four Over Six (4/6)" technical summary (Problem statement:
+// E2M1 steps and [-6,6] block scaling; Methodology: dual quantization, error,
+// selection; Implementation details: alpha over 256), "Pretraining Large
+// Language Models with NVFP4" sections 2b-2d (RHT, 2D scaling, stochastic
+// rounding), Salmon et al. SC'11 (Philox4x32-10).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace nvfp4 {
+
+constexpr float kAlphaDen = 2688.0f;    // 6 * 448: block max 6, E4M3 max 448
+constexpr float kAlphaDen46 = 1536.0f;  // 6 * 256: headroom for the 1.5x max-4 scale
+constexpr float kMinAmax = 0x1p-100f;   // below this the per-block reciprocal may overflow
+
+// status values written to the device status word (same integers as nvfp4.h)
+constexpr int kStatusNonFinite = -6;
+constexpr int kStatusRange = -7;
+
+// ---------------------------------------------------------------- bf16
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------- E4M3 scale
+// Scale byte of a non-negative ratio: round to nearest even, saturate at 448.
+__device__ __forceinline__ uint32_t e4m3_encode(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+// Value of a scale byte (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t e) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)e));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+}
+
+// ---------------------------------------------------------------- E2M1 codes
+// Two values -> one byte of codes (first value in the low nibble), round to
+// nearest even, saturating to +-6.
+__device__ __forceinline__ uint32_t e2m1x2(float first, float second) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}"
+      : "=r"(r)
+      : "f"(second), "f"(first));
+  return r;
+}
+
+// Eight values -> eight nibbles (value j in bits 4j..4j+3).
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Signed grid values of the two codes in the low byte of `byte2` (exact).
+__device__ __forceinline__ float2 e2m1x2_values(uint32_t byte2) {
+  uint32_t h2;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h2) : "r"(byte2));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+// ---------------------------------------------------------------- Philox4x32-10
+// Salmon et al., SC'11.  Counter (c0, c1, 0, 0), key (k0, k1); returns words
+// 0 and 1 of the output block.
+__device__ __forceinline__ uint2 philox_w01(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+  uint32_t c2 = 0u, c3 = 0u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint2(c0, c1);
+}
+
+// RHT sign bits: word 0 of Philox(key = seed, counter = (0,0,0,1)).
+__device__ __forceinline__ uint32_t rht_sign_bits(uint32_t k0, uint32_t k1) {
+  uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 1u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c0 & 0xFFFFu;
+}
+
+// ---------------------------------------------------------------- rounding
+// Stochastic rounding of v onto the E2M1 grid with block maximum Q: with
+// m = min(|v|, Q) between grid neighbours lo <= m < hi, return hi iff
+// (w >> 8) * 2^-24 < (m - lo) / (hi - lo); the sign of v is kept.  All steps
+// are exact (power-of-two step sizes).
+__device__ __forceinline__ float sr_round(float v, float Q, uint32_t w) {
+  const float m = fminf(fabsf(v), Q);
+  const float step = m < 2.0f ? 0.5f : (m < 4.0f ? 1.0f : 2.0f);
+  const float rstep = m < 2.0f ? 2.0f : (m < 4.0f ? 1.0f : 0.5f);
+  const float lo = __fmul_rn(floorf(__fmul_rn(m, rstep)), step);
+  const float p = __fmul_rn(__fsub_rn(m, lo), rstep);
+  const float u = __fmul_rn((float)(w >> 8), 0x1p-24f);
+  const float g = (u < p) ? __fadd_rn(lo, step) : lo;
+  return copysignf(g, v);
+}
+
+// ---------------------------------------------------------------- block scale
+struct BlockScale {
+  uint32_t e;  // E4M3 byte
+  float d;     // e * alpha
+  float inv;   // 1 / d (0 when d == 0: every code becomes a signed zero)
+};
+
+// b = block max, Q = 6 or 4:  t = b / (Q*alpha), e = E4M3(t), d = e*alpha.
+__device__ __forceinline__ BlockScale block_scale(float b, float alpha, float Q) {
+  BlockScale s;
+  const float den = __fmul_rn(Q, alpha);
+  const float t = (b > 0.0f) ? __fdiv_rn(b, den) : 0.0f;
+  s.e = e4m3_encode(t);
+  s.d = __fmul_rn(e4m3_value(s.e), alpha);
+  s.inv = (s.d != 0.0f) ? __frcp_rn(s.d) : 0.0f;
+  return s;
+}
+
+// ---------------------------------------------------------------- 4/6 error terms
+enum Sel : int { kSelMAE = 0, kSelMSE = 1, kSelMax = 2 };
+
+// Error term of one element: err = z - val*d rounded once (fma), then |err|
+// (MAE, MAX) or err*err (MSE).
+__device__ __forceinline__ float err_term(float z, float val, float d, int sel) {
+  const float err = __fmaf_rn(-val, d, z);
+  return (sel == kSelMSE) ? __fmul_rn(err, err) : fabsf(err);
+}
+
+// Combine two partial scores: a sum for MAE/MSE, a max for MAXERR.
+__device__ __forceinline__ float err_combine(float a, float b, int sel) {
+  return (sel == kSelMax) ? fmaxf(a, b) : __fadd_rn(a, b);
+}
+
+// Score of 8 consecutive elements whose codes are the 8 nibbles of `codes`,
+// summed as a perfect binary tree (adjacent pairs first).
+__device__ __forceinline__ float score8(const float* z, uint32_t codes, float d, int sel) {
+  float t[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 val = e2m1x2_values((codes >> (8 * j)) & 0xFFu);
+    t[2 * j] = err_term(z[2 * j], val.x, d, sel);
+    t[2 * j + 1] = err_term(z[2 * j + 1], val.y, d, sel);
+  }
+  const float a = err_combine(err_combine(t[0], t[1], sel), err_combine(t[2], t[3], sel), sel);
+  const float b = err_combine(err_combine(t[4], t[5], sel), err_combine(t[6], t[7], sel), sel);
+  return err_combine(a, b, sel);
+}
+
+// ---------------------------------------------------------------- Hadamard
+// In-register 16-point random Hadamard transform: y = (1/4) H16 (s . z) with
+// H16 in Sylvester order (the iterative butterfly yields natural order).
+__device__ __forceinline__ void rht16(float* z, uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if ((signs >> j) & 1u) z[j] = -z[j];
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = z[i], b = z[i + h];
+        z[i] = __fadd_rn(a, b);
+        z[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) z[j] = __fmul_rn(z[j], 0.25f);
+}
+
+// The same transform on a 16-vector split over a lane pair: the even lane
+// holds elements 0..7, the odd lane 8..15.  All 32 lanes must call it.
+__device__ __forceinline__ void rht16_pair(float* z, uint32_t signs, bool odd) {
+  const uint32_t s = odd ? (signs >> 8) : signs;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if ((s >> j) & 1u) z[j] = -z[j];
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float a = z[i], b = z[i + h];
+        z[i] = __fadd_rn(a, b);
+        z[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, z[j], 1);
+    // even lane: u[j] + u[j+8]; odd lane: u[j] - u[j+8] with u[j] the partner's
+    const float r = odd ? __fsub_rn(other, z[j]) : __fadd_rn(z[j], other);
+    z[j] = __fmul_rn(r, 0.25f);
+  }
+}
+
+// Status of a tensor amax: 0 if usable, else the status value.
+__device__ __forceinline__ int amax_status(float A) {
+  if (!(A <= 3.402823466e38f)) return kStatusNonFinite;  // Inf or NaN
+  if (A > 0.0f && A < kMinAmax) return kStatusRange;
+  return 0;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,62 @@
+// nvfp4_internal.h -- kernel launch interface shared by the library's own
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// One CTA covers a tile of kTileRows x kTileCols elements; each thread holds a
+// 16-row x 8-column register tile (sixteen 128-bit loads), a warp spans
+// 16 rows x 256 columns and the kWarps warps of a CTA are stacked vertically.
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileRows = kWarps * 16;
+constexpr int kTileCols = 256;
+
+struct QuantArgs {
+  const uint16_t* x;
+  int64_t M, N, ld;
+  const float* amax;  // [2]
+  float* alpha;       // [2]
+  int* status;        // nullable
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  uint64_t ctr_off;
+  uint32_t sr_k0, sr_k1;
+  uint32_t rht_k0, rht_k1;
+  int sel;
+  int rht_row, rht_col;
+};
+
+struct AmaxArgs {
+  const uint16_t* x;
+  int64_t M, N, ld;
+  uint32_t rht_k0, rht_k1;
+  float* amax;  // [2], zeroed before the launch
+};
+
+struct DequantArgs {
+  const uint8_t* q;
+  const uint8_t* s;
+  const float* alpha;
+  int64_t rows, cols;
+  int out_bf16;
+  void* out;
+};
+
+inline dim3 tile_grid(int64_t M, int64_t N) {
+  const int64_t gx = (N + kTileCols - 1) / kTileCols;
+  const int64_t gy = (M + kTileRows - 1) / kTileRows;
+  return dim3((unsigned)(gx > 0 ? gx : 1), (unsigned)(gy > 0 ? gy : 1), 1);
+}
+
+cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
+cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
+cudaError_t launch_quant2d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
+
+}  // namespace nvfp4

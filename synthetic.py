@@ -72,19 +72,28 @@ def gradient(M: int, N: int, seed: int, nu: float = 3.0, scale: float = 1e-3) ->
     return _fill(M, N, rng, lambda g, shape: (g.standard_t(nu, shape) * scale).astype(np.float32))
 
 
-# The five workloads of the recipe (name -> (generator, M, N, seed)).
+# The workloads of the recipe: name -> (generator, M, N, seed, flags, selection rule).
+# flags: 1 rowwise, 2 columnwise, 4 2D, 16 Hadamard on the columnwise copy,
+# 32 stochastic rounding, 64 4/6; selection 0 MAE, 1 MSE.
 WORKLOADS = {
-    "rowwise_rn_256x1024": (activation_outlier_entries, 256, 1024, DATA_SEED_BASE + 1),
-    "act_46mae_8192x5120": (activation_outlier_channels, 8192, 5120, DATA_SEED_BASE + 2),
-    "weight_2d_5120x20480": (weight, 5120, 20480, DATA_SEED_BASE + 3),
-    "grad_rht_sr_16384x5120": (gradient, 16384, 5120, DATA_SEED_BASE + 4),
-    "linear_x_16384x5120": (activation_outlier_channels, 16384, 5120, DATA_SEED_BASE + 5),
-    "linear_w_5120x20480": (weight, 5120, 20480, DATA_SEED_BASE + 6),
-    "linear_dy_16384x20480": (gradient, 16384, 20480, DATA_SEED_BASE + 7),
+    "rowwise_rn_256x1024": (activation_outlier_entries, 256, 1024, DATA_SEED_BASE + 1, 1, 0),
+    "act_46mae_8192x5120": (activation_outlier_channels, 8192, 5120, DATA_SEED_BASE + 2, 1 | 2 | 64, 0),
+    "weight_2d_5120x20480": (weight, 5120, 20480, DATA_SEED_BASE + 3, 1 | 2 | 4, 0),
+    "grad_rht_sr_16384x5120": (gradient, 16384, 5120, DATA_SEED_BASE + 4, 1 | 2 | 16 | 32, 0),
+    "linear_x_16384x5120": (activation_outlier_channels, 16384, 5120, DATA_SEED_BASE + 5, 1 | 2 | 64, 1),
+    "linear_w_5120x20480": (weight, 5120, 20480, DATA_SEED_BASE + 6, 1 | 2 | 4, 0),
+    "linear_dy_16384x20480": (gradient, 16384, 20480, DATA_SEED_BASE + 7, 1 | 2 | 16 | 32, 0),
 }
+SR_SEED = 0x1234ABCD
+RHT_SEED = 0x5EED
 
 
 def workload(name: str, M: int | None = None, N: int | None = None) -> np.ndarray:
     """The named workload's distribution at its own size, or at (M, N)."""
-    gen, M0, N0, seed = WORKLOADS[name]
+    gen, M0, N0, seed = WORKLOADS[name][:4]
     return gen(M or M0, N or N0, seed)
+
+
+def workload_flags(name: str):
+    """(flags, selection rule) of the named workload."""
+    return WORKLOADS[name][4], WORKLOADS[name][5]

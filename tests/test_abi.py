@@ -1,0 +1,123 @@
+"""The C-ABI library loads, exports what include/nvfp4.h declares, and rejects
+bad arguments on the host (no GPU needed: these calls return before any CUDA
+work is enqueued)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import nvfp4_bit_block_gb300 as nv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+ALIGNED = 0x100000       # fake, 16-byte aligned "device" addresses: never dereferenced
+ALIGNED2 = 0x200000
+ALIGNED3 = 0x300000
+
+
+@pytest.fixture(scope="module")
+def L():
+    nv.build()
+    return nv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*NVFP4_API\s+(?:int|const char\*)\s+(nvfp4_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_entry_points():
+    assert declared_functions() == ["nvfp4_amax", "nvfp4_dequantize", "nvfp4_quantize", "nvfp4_strerror"]
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", nv.build()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (nvfp4_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_library_is_built_for_sm_103a_only():
+    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", nv.build()], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_(\d+a?)", out.stdout))
+    assert arches == {"103a"}, arches
+
+
+def test_strerror(L):
+    assert nv.nvfp4_strerror(0) == "ok"
+    for st in (-1, -2, -3, -4, -5, -6, -7):
+        assert nv.nvfp4_strerror(st) not in ("", "unknown status")
+    assert nv.nvfp4_strerror(12345) == "unknown status"
+
+
+def quantize(L, x=ALIGNED, M=32, N=32, ld=32, amax=ALIGNED2, flags=3, sel=0,
+             q_row=ALIGNED, s_row=ALIGNED, q_col=ALIGNED, s_col=ALIGNED, alpha=ALIGNED3, status=None):
+    return L.nvfp4_quantize(x, M, N, ld, amax, flags, sel, 0, 0, 0, q_row, s_row, q_col, s_col, alpha,
+                            status, None)
+
+
+def test_quantize_rejects_bad_arguments(L):
+    assert quantize(L, flags=0) == -4                          # no copy requested
+    assert quantize(L, flags=3 | 128) == -4                    # unknown bit
+    assert quantize(L, flags=3 | 4 | 8) == -4                  # 2D with an RHT flag
+    assert quantize(L, flags=2 | 8) == -4                      # row RHT without the row copy
+    assert quantize(L, flags=1 | 16) == -4                     # col RHT without the col copy
+    assert quantize(L, flags=3 | 64, sel=3) == -4              # selection rule out of range
+    assert quantize(L, N=24, ld=24) == -2                      # N % 16
+    assert quantize(L, M=24) == -2                             # M % 16 with COLWISE
+    assert quantize(L, M=-16) == -2
+    assert quantize(L, ld=16) == -2                            # ld < N
+    assert quantize(L, N=32, ld=36) == -3                      # ld % 8
+    assert quantize(L, x=ALIGNED + 8) == -3                    # x not 16-byte aligned
+    assert quantize(L, q_row=ALIGNED + 4) == -3
+    assert quantize(L, s_col=ALIGNED + 1) == -3
+    assert quantize(L, amax=None) == -1
+    assert quantize(L, alpha=None) == -1
+    assert quantize(L, x=None) == -1
+    assert quantize(L, q_col=None) == -1
+    assert quantize(L, flags=1, q_col=None, s_col=None) != -1  # not needed without COLWISE
+    assert quantize(L, M=65536 * 128 + 16, flags=1) == -2      # beyond the row-tile grid limit
+
+
+def test_amax_and_dequantize_reject_bad_arguments(L):
+    assert L.nvfp4_amax(ALIGNED, 32, 24, 24, 1, 0, ALIGNED2, None) == -2
+    assert L.nvfp4_amax(ALIGNED, 32, 32, 32, 0, 0, ALIGNED2, None) == -4
+    assert L.nvfp4_amax(ALIGNED, 32, 32, 32, 1, 0, None, None) == -1
+    assert L.nvfp4_amax(ALIGNED + 2, 32, 32, 32, 1, 0, ALIGNED2, None) == -3
+    assert L.nvfp4_dequantize(ALIGNED, ALIGNED, ALIGNED2, 4, 24, 0, ALIGNED3, None) == -2
+    assert L.nvfp4_dequantize(None, ALIGNED, ALIGNED2, 4, 32, 0, ALIGNED3, None) == -1
+    assert L.nvfp4_dequantize(ALIGNED, ALIGNED, ALIGNED2, 4, 32, 0, ALIGNED3 + 8, None) == -3
+    assert L.nvfp4_dequantize(ALIGNED, ALIGNED, ALIGNED2, 0, 32, 0, ALIGNED3, None) == 0  # empty: no-op
+
+
+def test_launch_failure_is_reported(L):
+    """The launch wrapper maps a CUDA failure to NVFP4_ERR_CUDA; the test hook
+    makes the next launch fail without touching a GPU."""
+    hook = L.nvfp4_test_fail_next_launch
+    hook.restype = None
+    hook()
+    assert quantize(L) == -5
+    hook()
+    assert L.nvfp4_amax(ALIGNED, 32, 32, 32, 1, 0, ALIGNED2, None) == -5
+    hook()
+    assert L.nvfp4_dequantize(ALIGNED, ALIGNED, ALIGNED2, 4, 32, 0, ALIGNED3, None) == -5
+
+
+def test_binding_raises_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(nv, "_lib", None)
+    monkeypatch.setattr(nv, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        nv.lib()
+
+
+def test_binding_has_the_c_names():
+    for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_strerror"):
+        assert callable(getattr(nv, name))

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small cases span several CTA tiles (128 x 256) plus ragged tails and are
+compared element by element; the recipe's full-size workloads run in the
+launch configuration the benchmark times and are compared on sampled 16-row
+stripes that the oracle computes one by one.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_bit_block_gb300 as nv
+import oracle
+import synthetic
+from gpu_helpers import (assert_copy_exact, assert_parity, gpu_quantize, ref_quantize, to_device,
+                         signed_grid_index)
+
+pytestmark = pytest.mark.gpu
+
+ROW, COL, TWO_D, RHT_ROW, RHT_COL, SR, F46 = 1, 2, 4, 8, 16, 32, 64
+VALID_FLAGS = [f for f in range(128)
+               if (f & 3) and not ((f & TWO_D) and (f & (RHT_ROW | RHT_COL)))
+               and not ((f & RHT_ROW) and not (f & ROW)) and not ((f & RHT_COL) and not (f & COL))]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    nv.build()
+    oracle.build()
+
+
+def small_input(M=272, N=528, kind="act"):
+    if kind == "act":
+        bits = synthetic.activation_outlier_channels(M, N, 11, frac=0.01)
+    elif kind == "grad":
+        bits = synthetic.gradient(M, N, 12)
+    else:
+        bits = synthetic.weight(M, N, 13)
+    f = bits.view(np.uint16).copy()
+    # degenerate blocks: an all-zero 16x16 tile, a tiny block, negative zeros
+    f[16:32, 32:48] = 0
+    f[40, 64:80] = 0x0001                       # bf16 2^-133 next to O(1) values
+    f[50, 100] = 0x8000
+    return f
+
+
+@pytest.mark.parametrize("flags", VALID_FLAGS)
+def test_every_flag_combination_small(flags):
+    sels = (0, 1, 2) if flags & F46 else (0,)
+    kind = "grad" if flags & (SR | RHT_ROW | RHT_COL) else ("weight" if flags & TWO_D else "act")
+    bits = small_input(kind=kind)
+    x = to_device(bits)
+    for sel in sels:
+        g = gpu_quantize(x, flags, sel, sr_seed=0x1234ABCD, rht_seed=0x5EED, counter_offset=3)
+        r = ref_quantize(bits, flags, sel, sr_seed=0x1234ABCD, rht_seed=0x5EED, counter_offset=3)
+        assert_parity(g, r, flags)
+
+
+@pytest.mark.parametrize("flags", [ROW, ROW | F46, ROW | SR, ROW | RHT_ROW | SR | F46])
+@pytest.mark.parametrize("M", [1, 7, 261])
+def test_rowwise_only_ragged_rows(flags, M):
+    bits = synthetic.activation_outlier_entries(M, 272, 21)
+    g = gpu_quantize(to_device(bits), flags, 1, sr_seed=5, rht_seed=6)
+    r = ref_quantize(bits, flags, 1, sr_seed=5, rht_seed=6)
+    assert_parity(g, r, flags)
+
+
+@pytest.mark.parametrize("flags", [ROW | COL | F46, ROW | COL | TWO_D, ROW | COL | RHT_COL | SR])
+def test_padded_leading_dimension(flags):
+    bits = small_input(144, 272)
+    x = to_device(bits, ld=312)
+    assert x.stride(0) == 312
+    g = gpu_quantize(x, flags, 0, sr_seed=1, rht_seed=2)
+    r = ref_quantize(bits, flags, 0, sr_seed=1, rht_seed=2)
+    assert_parity(g, r, flags)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (16, 256), (32, 16), (128, 256), (144, 2064)])
+def test_tile_edges(shape):
+    bits = synthetic.activation_outlier_channels(*shape, 31, frac=0.05)
+    for flags in (ROW | COL | F46, ROW | COL | TWO_D | F46, ROW | COL | RHT_COL | SR):
+        g = gpu_quantize(to_device(bits), flags, 2, sr_seed=9, rht_seed=10)
+        r = ref_quantize(bits, flags, 2, sr_seed=9, rht_seed=10)
+        assert_parity(g, r, flags)
+
+
+def test_extreme_magnitudes():
+    """bf16 values near the top of the range, subnormal inputs and blocks whose
+    scale underflows E4M3 (subnormal and zero scale bytes)."""
+    rs = np.random.default_rng(3)
+    f = (rs.standard_normal((64, 256)) * 1e-3).astype(np.float32)
+    f[0, 0] = 3.0e38                                       # amax near bf16 max
+    f[1, :16] = 1e30
+    f[2, :] = rs.standard_normal(256).astype(np.float32) * 1e-36   # bf16 subnormal range
+    bits = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for flags in (ROW | COL, ROW | COL | F46, ROW | COL | TWO_D, ROW | COL | SR, ROW | COL | F46 | SR):
+        for sel in (0, 1, 2):
+            g = gpu_quantize(to_device(bits), flags, sel, sr_seed=4)
+            r = ref_quantize(bits, flags, sel, sr_seed=4)
+            assert_parity(g, r, flags)
+
+
+def test_zero_and_empty_tensors():
+    bits = np.zeros((32, 48), np.uint16)
+    bits[3, 5] = 0x8000
+    for flags in (ROW | COL, ROW | COL | F46 | SR, ROW | COL | TWO_D):
+        g = gpu_quantize(to_device(bits), flags)
+        r = ref_quantize(bits, flags)
+        assert_parity(g, r, flags)
+        assert g["alpha"][0] == 0 and not g["s_row"].any()
+    empty = torch.zeros((0, 32), dtype=torch.bfloat16, device="cuda")
+    amax = nv.nvfp4_amax(empty, ROW)
+    out = nv.nvfp4_quantize(empty, amax, ROW)
+    torch.cuda.synchronize()
+    assert amax.cpu().tolist() == [0.0, 0.0] and out.alpha.cpu().tolist() == [0.0, 0.0]
+
+
+def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
+    for pattern, want in ((0x7F80, -6), (0xFFC0, -6)):
+        bits = synthetic.weight(32, 32, 1)
+        bits[5, 7] = pattern
+        x = to_device(bits)
+        amax = nv.nvfp4_amax(x, ROW | COL)
+        out = nv.Quantized(*(torch.full(s, 0xAB, dtype=torch.uint8, device="cuda")
+                             for s in nv.output_shapes(32, 32, ROW | COL)),
+                           alpha=torch.zeros(2, device="cuda"), status=torch.zeros(1, dtype=torch.int32,
+                                                                                   device="cuda"))
+        nv.nvfp4_quantize(x, amax, ROW | COL, out=out)
+        torch.cuda.synchronize()
+        assert out.status.item() == want
+        assert bool((out.q_row == 0xAB).all()) and bool((out.s_col == 0xAB).all())
+        st, am = oracle.amax(bits, ROW | COL)
+        assert oracle.quantize(bits, 32, am, ROW | COL)["status"] == want
+    tiny = np.full((32, 32), 0x0001, np.uint16)
+    g = gpu_quantize(to_device(tiny), ROW)
+    assert g["status"] == -7
+    st, am = oracle.amax(tiny, ROW)
+    assert oracle.quantize(tiny, 32, am, ROW)["status"] == -7
+
+
+def test_two_d_copies_are_transposes_and_dequantize_identically():
+    bits = synthetic.weight(256, 512, 17)
+    for flags in (ROW | COL | TWO_D, ROW | COL | TWO_D | F46, ROW | COL | TWO_D | SR):
+        g = gpu_quantize(to_device(bits), flags, 0, sr_seed=8)
+        unpack = lambda q: np.stack([q & 15, q >> 4], -1).reshape(q.shape[0], -1)
+        assert np.array_equal(unpack(g["q_col"]), unpack(g["q_row"]).T)
+        out = g["_out"]
+        dr = nv.nvfp4_dequantize(out.q_row, out.s_row, out.alpha[0:1])
+        dc = nv.nvfp4_dequantize(out.q_col, out.s_col, out.alpha[1:2])
+        assert torch.equal(dc.T.contiguous().view(torch.int32), dr.view(torch.int32))
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_dequantize_matches_oracle(bf16):
+    bits = small_input()
+    flags = ROW | COL | F46
+    g = gpu_quantize(to_device(bits), flags, 0)
+    out = g["_out"]
+    for q, s, a, (rows, cols) in ((out.q_row, out.s_row, out.alpha[0:1], bits.shape),
+                                  (out.q_col, out.s_col, out.alpha[1:2], bits.shape[::-1])):
+        d = nv.nvfp4_dequantize(q, s, a, out_dtype=torch.bfloat16 if bf16 else torch.float32)
+        torch.cuda.synchronize()
+        ref = oracle.dequantize(q.cpu().numpy(), s.cpu().numpy(), float(a.item()), rows, cols, out_bf16=bf16)
+        got = d.cpu().view(torch.int16 if bf16 else torch.int32).numpy()
+        assert np.array_equal(got, ref.view(np.int16 if bf16 else np.int32))
+
+
+def test_counter_offset_reproduces_a_row_shard():
+    bits = synthetic.gradient(256, 512, 23)
+    flags = ROW | COL | RHT_COL | SR
+    x = to_device(bits)
+    amax = nv.nvfp4_amax(x, flags, 77)
+    whole = gpu_quantize(x, flags, 0, sr_seed=41, rht_seed=77, amax=amax)
+    shard = gpu_quantize(x[128:], flags, 0, sr_seed=41, rht_seed=77, counter_offset=128 * 512, amax=amax)
+    assert np.array_equal(shard["q_row"], whole["q_row"][128:])
+    assert np.array_equal(shard["q_col"], whole["q_col"][:, 64:])
+    assert np.array_equal(shard["s_col"], whole["s_col"][:, 8:])
+
+
+def test_deterministic_and_graph_capturable():
+    bits = small_input()
+    flags = ROW | COL | RHT_COL | SR
+    x = to_device(bits)
+    a = gpu_quantize(x, flags, 0, sr_seed=3, rht_seed=4)
+    b = gpu_quantize(x, flags, 0, sr_seed=3, rht_seed=4)
+    for k in ("q_row", "s_row", "q_col", "s_col", "amax", "alpha"):
+        assert np.array_equal(a[k], b[k])
+    s = torch.cuda.Stream()
+    amax = torch.empty(2, dtype=torch.float32, device="cuda")
+    out = nv.nvfp4_quantize(x, a["_amax"], flags, 0, 3, 4)  # allocate outputs outside the capture
+    torch.cuda.synchronize()
+    for t in (out.q_row, out.q_col):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nv.nvfp4_amax(x, flags, 4, out=amax)
+        nv.nvfp4_quantize(x, amax, flags, 0, 3, 4, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.q_row.cpu().numpy(), a["q_row"])
+    assert np.array_equal(out.q_col.cpu().numpy(), a["q_col"])
+
+
+# ------------------------------------------------------------------ full-size workloads
+STRIPES = 6
+
+
+@pytest.mark.parametrize("name", list(synthetic.WORKLOADS))
+def test_workload_full_size_sampled(name):
+    flags, sel = synthetic.workload_flags(name)
+    bits = synthetic.workload(name)
+    M, N = bits.shape
+    x = to_device(bits)
+    g = gpu_quantize(x, flags, sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED)
+    del x
+    st, am = oracle.amax(bits, flags, synthetic.RHT_SEED)
+    if M * N <= 1 << 20:
+        r = oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED)
+        r["amax"] = am
+        assert_parity(g, r, flags)
+        return
+    rs = np.random.default_rng(zlib.crc32(name.encode()))
+    stripes = sorted(set([0, M // 16 - 1] + list(rs.integers(0, M // 16, STRIPES))))
+    outs = oracle.output_buffers(M, N, flags)
+    for sidx in stripes:
+        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
+                        row0=16 * sidx, row1=16 * sidx + 16, outs=outs)
+    q_row, s_row, q_col, s_col = outs
+    rows = np.concatenate([np.arange(16 * s, 16 * s + 16) for s in stripes])
+    gs = dict(amax=g["amax"], alpha=g["alpha"], status=g["status"],
+              q_row=g["q_row"][rows], s_row=g["s_row"][rows],
+              q_col=np.concatenate([g["q_col"][:, 8 * s:8 * s + 8] for s in stripes], 1),
+              s_col=g["s_col"][:, stripes])
+    alpha = np.zeros(2, np.float32)
+    den = np.float32(1536.0 if flags & F46 else 2688.0)
+    alpha[:] = am / den
+    rr = dict(amax=am, alpha=alpha, q_row=q_row[rows], s_row=s_row[rows],
+              q_col=np.concatenate([q_col[:, 8 * s:8 * s + 8] for s in stripes], 1), s_col=s_col[:, stripes])
+    assert_parity(gs, rr, flags)
