@@ -29,8 +29,8 @@ int check_shape(int64_t M, int64_t N, int64_t ld, uint32_t flags) {
   if ((flags & (NVFP4_COLWISE | NVFP4_2D)) && (M % 16)) return NVFP4_ERR_SHAPE;
   if (ld < N) return NVFP4_ERR_SHAPE;
   if (ld % 8) return NVFP4_ERR_ALIGN;
-  // grid limit: the row tiles go into gridDim.y
-  if ((M + nvfp4::kTileRows - 1) / nvfp4::kTileRows > 65535) return NVFP4_ERR_SHAPE;
+  // grid limit: row tiles (64 rows for the 1D kernels) go into gridDim.y
+  if ((M + 63) / 64 > 65535) return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
 }
 

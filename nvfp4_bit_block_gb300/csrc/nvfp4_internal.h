@@ -7,14 +7,6 @@
 
 namespace nvfp4 {
 
-// One CTA covers a tile of kTileRows x kTileCols elements; each thread holds a
-// 16-row x 8-column register tile (sixteen 128-bit loads), a warp spans
-// 16 rows x 256 columns and the kWarps warps of a CTA are stacked vertically.
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kTileRows = kWarps * 16;
-constexpr int kTileCols = 256;
-
 struct QuantArgs {
   const uint16_t* x;
   int64_t M, N, ld;
@@ -47,12 +39,6 @@ struct DequantArgs {
   int out_bf16;
   void* out;
 };
-
-inline dim3 tile_grid(int64_t M, int64_t N) {
-  const int64_t gx = (N + kTileCols - 1) / kTileCols;
-  const int64_t gy = (M + kTileRows - 1) / kTileRows;
-  return dim3((unsigned)(gx > 0 ? gx : 1), (unsigned)(gy > 0 ? gy : 1), 1);
-}
 
 cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);

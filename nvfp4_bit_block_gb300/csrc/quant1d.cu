@@ -1,48 +1,127 @@
 // quant1d.cu -- fused rowwise + columnwise NVFP4 quantization with 1x16 blocks.
 //
-// One read of X produces both copies: each thread loads a 16-row x 8-column
-// register tile with sixteen coalesced 128-bit loads.  Rowwise blocks (16
-// consecutive columns) span a lane pair and combine with one shuffle;
-// columnwise blocks (16 consecutive rows of one column) lie entirely in one
-// thread, so the transposed copy needs no shared-memory transpose.
+// One read of X produces both copies.  Persistent CTAs stream 64 x 256 bf16
+// tiles through double-buffered shared memory (tile_pipeline.cuh), then
+//   - the rowwise pass gives each thread whole 16-column blocks (two 128-bit
+//     shared loads) and stores their codes directly (coalesced), and
+//   - the columnwise pass gives each thread a column pair over 16 rows (sixteen
+//     32-bit shared loads, one bf16x2 word per row) and stages the codes, so
+//     that each column of the transposed copy is written as one 32-byte store,
+// so every block's scale, rounding and 4/6 choice happen in one thread's
+// registers.  Element arithmetic uses packed f32x2 operations.
+//
+// With stochastic rounding on both copies, one Philox4x32-10 call per element
+// serves both: the rowwise pass uses word 0 and parks word 1 in shared memory
+// for the columnwise pass.
 //
 // Sources: "Four Over Six (4/6)" technical summary (Problem statement,
 // Methodology, Implementation details) and "Pretraining Large Language Models
 // with NVFP4" sections 1, 2b and 2d.
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
+#include "tile_pipeline.cuh"
 
 namespace nvfp4 {
 namespace {
 
-// Codes of 8 values of one block at scale s (block maximum Q): RN through the
-// saturating cvt (clamped to +-4 first when a max-4 scale is subnormal and
-// |v| could exceed 5), or SR with the given words.
-template <bool SR>
-__device__ __forceinline__ uint32_t quant8(const float* z, const BlockScale& s, float Q,
-                                           const uint32_t* w) {
-  float v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(z[j], s.inv);
-  if (SR) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = sr_round(v[j], Q, w[j]);
-  } else if (Q == 4.0f && s.e < 8u) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
-  }
-  return e2m1x8(v);
-}
+using tile::kTM;
+using tile::kTN;
+constexpr int kStashBytes = kTM * kTN * 4;  // Philox word 1 per element, 64 KB
+constexpr int kBlockThreads = 256;
+
+// 16-byte chunk q of a stash row (64 chunks) lives at chunk q ^ ((q >> 3) & 7)
+__device__ __forceinline__ int swz_stash(int q) { return q ^ ((q >> 3) & 7); }
 
 __device__ __forceinline__ uint2 ctr_of(uint64_t i) { return make_uint2((uint32_t)i, (uint32_t)(i >> 32)); }
 
+// Codes of 16 values at block scale s (block maximum Q), nibbles in element
+// order.  RN goes through the saturating cvt (a max-4 candidate whose scale
+// byte is subnormal is clamped to +-4 first, since |v| may then exceed 5);
+// SR rounds with the given Philox words.
+template <bool SR>
+__device__ __forceinline__ uint2 codes16(const float* z, const BlockScale& s, float Q, const uint32_t* w) {
+  float v[16];
+  const float2 inv2 = make_float2(s.inv, s.inv);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
+    v[2 * j] = r.x;
+    v[2 * j + 1] = r.y;
+  }
+  if (SR) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = sr_round(v[j], Q, w[j]);
+  } else if (Q == 4.0f && s.e < 8u) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
+  }
+  return make_uint2(e2m1x8(v), e2m1x8(v + 8));
+}
+
+// 4/6 score of a 16-value block: err = z - val*d rounded once; MAE sums |err|,
+// MSE sums err*err, both over the perfect binary tree in block order;
+// MAXERR takes max |err|.
+__device__ __forceinline__ float score16(const float* z, uint2 codes, float d, int sel) {
+  const float2 nd = make_float2(-d, -d);
+  float e[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t word = (j < 4) ? codes.x : codes.y;
+    const float2 val = e2m1x2_values((word >> (8 * (j & 3))) & 0xFFu);
+    const float2 err = fma2(val, nd, make_float2(z[2 * j], z[2 * j + 1]));
+    e[2 * j] = err.x;
+    e[2 * j + 1] = err.y;
+  }
+  if (sel == kSelMax) {
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(e[j]));
+    return m;
+  }
+  float t[8];
+  if (sel == kSelMSE) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 sq = mul2(make_float2(e[2 * j], e[2 * j + 1]), make_float2(e[2 * j], e[2 * j + 1]));
+      t[j] = __fadd_rn(sq.x, sq.y);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = __fadd_rn(fabsf(e[2 * j]), fabsf(e[2 * j + 1]));
+  }
+  // ((t0+t1)+(t2+t3)) + ((t4+t5)+(t6+t7)), two sums per packed add
+  const float2 a = add2(make_float2(t[0], t[4]), make_float2(t[1], t[5]));
+  const float2 b = add2(make_float2(t[2], t[6]), make_float2(t[3], t[7]));
+  const float2 c = add2(a, b);
+  return __fadd_rn(c.x, c.y);
+}
+
+// One block: the standard max-6 candidate and, with 4/6, the max-4 candidate;
+// the max-4 one is kept only if its score is strictly lower.
+template <bool Q46, bool SR>
+__device__ __forceinline__ void quant_block16(const float* z, float bmax, float alpha, int sel,
+                                              const uint32_t* w, uint2& codes, uint32_t& e) {
+  const BlockScale s6 = block_scale(bmax, alpha, 6.0f);
+  codes = codes16<SR>(z, s6, 6.0f, w);
+  e = s6.e;
+  if (Q46) {
+    const BlockScale s4 = block_scale(bmax, alpha, 4.0f);
+    const uint2 c4 = codes16<SR>(z, s4, 4.0f, w);
+    if (score16(z, c4, s4.d, sel) < score16(z, codes, s6.d, sel)) {
+      codes = c4;
+      e = s4.e;
+    }
+  }
+}
+
 template <bool ROW, bool COL, bool Q46, bool SR>
-__global__ void __launch_bounds__(kThreads) quant1d_kernel(const QuantArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const bool odd = (lane & 1) != 0;
-  const int64_t r0 = ((int64_t)blockIdx.y * kWarps + warp) * 16;
-  const int64_t c0 = (int64_t)blockIdx.x * kTileCols + lane * 8;
+__global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr bool kStash = SR && ROW && COL;
+  uint8_t* bufs = smem;                                      // 2 x 32 KB tiles
+  uint8_t* cstage = smem + 2 * tile::kTileBytes;             // 8 KB
+  uint8_t* sstage = cstage + tile::kCStageBytes;             // 1 KB
+  uint8_t* stash = sstage + tile::kSStageBytes;              // 64 KB with kStash
 
   // a2: alpha = amax / (6*448), or amax / (6*256) with 4/6
   const float den = Q46 ? kAlphaDen46 : kAlphaDen;
@@ -51,211 +130,178 @@ __global__ void __launch_bounds__(kThreads) quant1d_kernel(const QuantArgs a) {
   const float alpha_c = __fdiv_rn(A_c, den);
   const int st_r = ROW ? amax_status(A_r) : 0;
   const int st_c = COL ? amax_status(A_c) : 0;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.alpha[0] = alpha_r;
     a.alpha[1] = alpha_c;
     if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
   }
   if (st_r || st_c) return;
-  if (r0 >= a.M) return;  // whole warp beyond the tensor
 
-  const bool col_ok = c0 < a.N;
+  const int64_t M = a.M, N = a.N;
+  const int64_t ntx = (N + kTN - 1) / kTN;
+  const int64_t ntiles = ((M + kTM - 1) / kTM) * ntx;
+  const int tid = threadIdx.x;
+  const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
   const int sel = a.sel;
 
-  // a3: one read of the 16x8 register tile
-  uint32_t xr[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (col_ok && r0 + i < a.M) v = ld_stream(a.x + (r0 + i) * a.ld + c0);
-    xr[i][0] = v.x;
-    xr[i][1] = v.y;
-    xr[i][2] = v.z;
-    xr[i][3] = v.w;
-  }
-  const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
-  const int64_t N = a.N, M = a.M;
+  int64_t t = blockIdx.x;
+  if (t < ntiles) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, tile::coord(t, ntx), tid);
+  tile::commit();
+  for (int it = 0; t < ntiles; t += gridDim.x, ++it) {
+    uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
+    const int64_t tn = t + gridDim.x;
+    if (tn < ntiles)  // prefetch the next tile into the other buffer
+      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld,
+                                      tile::coord(tn, ntx), tid);
+    tile::commit();
+    tile::wait_all_but_one();
+    __syncthreads();
+    const tile::Coord tc = tile::coord(t, ntx);
 
-  // Stochastic rounding without 4/6 and without a rowwise transform: one
-  // Philox call per element feeds both copies (word 0 rowwise, word 1
-  // columnwise) in a single sweep over column pairs.
-  constexpr bool kFusedSR = SR && !Q46 && ROW && COL;
-  if (kFusedSR && !a.rht_row) {
-    float invR[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float b = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) b = fmaxf(b, fmaxf(fabsf(bf16_lo(xr[i][k])), fabsf(bf16_hi(xr[i][k]))));
-      b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
-      const BlockScale s = block_scale(b, alpha_r, 6.0f);
-      invR[i] = s.inv;
-      if (col_ok && !odd) a.s_row[(r0 + i) * (N / 16) + c0 / 16] = (uint8_t)s.e;
-    }
-    uint32_t rq[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) rq[i] = 0u;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float z0[16], z1[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        z0[i] = bf16_lo(xr[i][k]);
-        z1[i] = bf16_hi(xr[i][k]);
-      }
-      if (a.rht_col) {
-        rht16(z0, signs);
-        rht16(z1, signs);
-      }
-      float b0 = 0.0f, b1 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        b0 = fmaxf(b0, fabsf(z0[i]));
-        b1 = fmaxf(b1, fabsf(z1[i]));
-      }
-      const BlockScale sc0 = block_scale(b0, alpha_c, 6.0f);
-      const BlockScale sc1 = block_scale(b1, alpha_c, 6.0f);
-      const int64_t ca = c0 + 2 * k, cb = ca + 1;
-      uint32_t cqa[2] = {0u, 0u}, cqb[2] = {0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const uint64_t base0 = a.ctr_off + (uint64_t)(r0 + i) * (uint64_t)N + (uint64_t)ca;
-        const uint64_t base1 = base0 + (uint64_t)N;
-        const uint2 c00 = ctr_of(base0), c01 = ctr_of(base0 + 1), c10 = ctr_of(base1), c11 = ctr_of(base1 + 1);
-        const uint2 w00 = philox_w01(c00.x, c00.y, a.sr_k0, a.sr_k1);  // (i,   ca)
-        const uint2 w01 = philox_w01(c01.x, c01.y, a.sr_k0, a.sr_k1);  // (i,   cb)
-        const uint2 w10 = philox_w01(c10.x, c10.y, a.sr_k0, a.sr_k1);  // (i+1, ca)
-        const uint2 w11 = philox_w01(c11.x, c11.y, a.sr_k0, a.sr_k1);  // (i+1, cb)
-        // rowwise codes (word 0), values are the untransformed x
-        const float r00 = sr_round(__fmul_rn(bf16_lo(xr[i][k]), invR[i]), 6.0f, w00.x);
-        const float r01 = sr_round(__fmul_rn(bf16_hi(xr[i][k]), invR[i]), 6.0f, w01.x);
-        const float r10 = sr_round(__fmul_rn(bf16_lo(xr[i + 1][k]), invR[i + 1]), 6.0f, w10.x);
-        const float r11 = sr_round(__fmul_rn(bf16_hi(xr[i + 1][k]), invR[i + 1]), 6.0f, w11.x);
-        rq[i] |= e2m1x2(r00, r01) << (8 * k);
-        rq[i + 1] |= e2m1x2(r10, r11) << (8 * k);
-        // columnwise codes (word 1)
-        const float g0a = sr_round(__fmul_rn(z0[i], sc0.inv), 6.0f, w00.y);
-        const float g1a = sr_round(__fmul_rn(z0[i + 1], sc0.inv), 6.0f, w10.y);
-        const float g0b = sr_round(__fmul_rn(z1[i], sc1.inv), 6.0f, w01.y);
-        const float g1b = sr_round(__fmul_rn(z1[i + 1], sc1.inv), 6.0f, w11.y);
-        cqa[i / 8] |= e2m1x2(g0a, g1a) << (8 * ((i / 2) % 4));
-        cqb[i / 8] |= e2m1x2(g0b, g1b) << (8 * ((i / 2) % 4));
-      }
-      if (col_ok) {
-        *reinterpret_cast<uint2*>(a.q_col + ca * (M / 2) + r0 / 2) = make_uint2(cqa[0], cqa[1]);
-        *reinterpret_cast<uint2*>(a.q_col + cb * (M / 2) + r0 / 2) = make_uint2(cqb[0], cqb[1]);
-        a.s_col[ca * (M / 16) + r0 / 16] = (uint8_t)sc0.e;
-        a.s_col[cb * (M / 16) + r0 / 16] = (uint8_t)sc1.e;
-      }
-    }
-    if (col_ok) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<uint32_t*>(a.q_row + (r0 + i) * (N / 2) + c0 / 2) = rq[i];
-    }
-    return;
-  }
-
-  // ---- rowwise copy: blocks of 16 columns, split over a lane pair
-  if (ROW) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int64_t r = r0 + i;
-      if (r >= M) break;  // same row for every lane of the warp
-      float z[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        z[2 * k] = bf16_lo(xr[i][k]);
-        z[2 * k + 1] = bf16_hi(xr[i][k]);
-      }
-      if (a.rht_row) rht16_pair(z, signs, odd);
-      float b = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(z[j]));
-      b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
-      uint32_t w[8];
-      if (SR) {
+    // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
+    if (ROW) {
+#pragma unroll 1
+      for (int k = 0; k < kTM * 16 / kBlockThreads; ++k) {
+        const int task = tid + k * kBlockThreads;
+        const int r = task >> 4, b = task & 15;
+        const int64_t grow = tc.R0 + r, gcol = tc.C0 + 16 * b;
+        if (grow >= M || gcol >= N) continue;
+        uint32_t wd[8];
+        tile::read_row_block(buf, r, b, wd);
+        float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint2 c = ctr_of(a.ctr_off + (uint64_t)r * (uint64_t)N + (uint64_t)(c0 + j));
-          w[j] = philox_w01(c.x, c.y, a.sr_k0, a.sr_k1).x;
+          z[2 * j] = bf16_lo(wd[j]);
+          z[2 * j + 1] = bf16_hi(wd[j]);
         }
-      }
-      const BlockScale s6 = block_scale(b, alpha_r, 6.0f);
-      uint32_t codes = quant8<SR>(z, s6, 6.0f, w);
-      uint32_t e = s6.e;
-      if (Q46) {
-        const BlockScale s4 = block_scale(b, alpha_r, 4.0f);
-        const uint32_t codes4 = quant8<SR>(z, s4, 4.0f, w);
-        float sc6 = score8(z, codes, s6.d, sel);
-        float sc4 = score8(z, codes4, s4.d, sel);
-        sc6 = err_combine(sc6, __shfl_xor_sync(0xFFFFFFFFu, sc6, 1), sel);
-        sc4 = err_combine(sc4, __shfl_xor_sync(0xFFFFFFFFu, sc4, 1), sel);
-        if (sc4 < sc6) {
-          codes = codes4;
-          e = s4.e;
+        float bmax;
+        if (a.rht_row) {
+          rht16(z, signs);
+          bmax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(z[j]));
+        } else {
+          bmax = block_absmax16(wd);
         }
-      }
-      if (col_ok) {
-        *reinterpret_cast<uint32_t*>(a.q_row + r * (N / 2) + c0 / 2) = codes;
-        if (!odd) a.s_row[r * (N / 16) + c0 / 16] = (uint8_t)e;
+        uint32_t w[16];
+        if (SR) {
+          const uint64_t base = a.ctr_off + (uint64_t)grow * (uint64_t)N + (uint64_t)gcol;
+          uint32_t w1[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint2 c = ctr_of(base + j);
+            const uint2 pw = philox_w01(c.x, c.y, a.sr_k0, a.sr_k1);
+            w[j] = pw.x;
+            w1[j] = pw.y;
+          }
+          if (kStash) {
+            uint8_t* srow = stash + r * (kTN * 4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(srow + swz_stash(4 * b + q) * 16) =
+                  make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+          }
+        }
+        uint2 codes;
+        uint32_t e;
+        quant_block16<Q46, SR>(z, bmax, alpha_r, sel, w, codes, e);
+        *reinterpret_cast<uint2*>(a.q_row + grow * (N / 2) + gcol / 2) = codes;
+        a.s_row[grow * (N / 16) + gcol / 16] = (uint8_t)e;
       }
     }
-  }
+    if (kStash) __syncthreads();
 
-  // ---- columnwise copy: blocks of 16 rows of one column, all in this thread
-  if (COL) {
+    // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
+    if (COL) {
+#pragma unroll 1
+      for (int k = 0; k < (kTN / 2) * (kTM / 16) / kBlockThreads; ++k) {
+        const int task = tid + k * kBlockThreads;
+        const int p = task & 127, rb = task >> 7;
+        const int64_t gcol = tc.C0 + 2 * p, grow0 = tc.R0 + 16 * rb;
+        if (gcol >= N || grow0 >= M) continue;
+        uint32_t wd[16];
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const int k = cc >> 1;
-      float z[16];
-      if (cc & 1) {
+        for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, p);
+        // both columns' maxima at once (low half = column 2p, high half = 2p+1)
+        uint32_t m2 = 0u;
+        if (!a.rht_col) {
+          uint32_t t8[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = bf16_hi(xr[i][k]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = bf16_lo(xr[i][k]);
-      }
-      const int64_t c = c0 + cc;
-      if (a.rht_col) rht16(z, signs);
-      float b = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(z[i]));
-      uint32_t w[16];
-      if (SR) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint2 ct = ctr_of(a.ctr_off + (uint64_t)(r0 + i) * (uint64_t)N + (uint64_t)c);
-          w[i] = philox_w01(ct.x, ct.y, a.sr_k0, a.sr_k1).y;
+          for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(wd[2 * i], wd[2 * i + 1]);
+          m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(t8[0], t8[1]), absmax_bf16x2(t8[2], t8[3])),
+                             absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7]))) &
+               0x7FFF7FFFu;
         }
-      }
-      const BlockScale s6 = block_scale(b, alpha_c, 6.0f);
-      uint32_t lo = quant8<SR>(z, s6, 6.0f, w);
-      uint32_t hi = quant8<SR>(z + 8, s6, 6.0f, w + 8);
-      uint32_t e = s6.e;
-      if (Q46) {
-        const BlockScale s4 = block_scale(b, alpha_c, 4.0f);
-        const uint32_t lo4 = quant8<SR>(z, s4, 4.0f, w);
-        const uint32_t hi4 = quant8<SR>(z + 8, s4, 4.0f, w + 8);
-        const float sc6 = err_combine(score8(z, lo, s6.d, sel), score8(z + 8, hi, s6.d, sel), sel);
-        const float sc4 = err_combine(score8(z, lo4, s4.d, sel), score8(z + 8, hi4, s4.d, sel), sel);
-        if (sc4 < sc6) {
-          lo = lo4;
-          hi = hi4;
-          e = s4.e;
+        uint2 codes[2];
+        uint32_t es[2];
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = h ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
+          float bmax = h ? bf16_hi(m2) : bf16_lo(m2);
+          if (a.rht_col) {
+            rht16(z, signs);
+            bmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(z[i]));
+          }
+          const int cc = 2 * p + h;  // tile column
+          uint32_t w[16];
+          if (SR) {
+            if (kStash) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = *reinterpret_cast<const uint32_t*>(stash + (16 * rb + i) * (kTN * 4) +
+                                                          swz_stash(cc >> 2) * 16 + (cc & 3) * 4);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const uint2 ct = ctr_of(a.ctr_off + (uint64_t)(grow0 + i) * (uint64_t)N + (uint64_t)(gcol + h));
+                w[i] = philox_w01(ct.x, ct.y, a.sr_k0, a.sr_k1).y;
+              }
+            }
+          }
+          uint2 cd;
+          uint32_t e;
+          quant_block16<Q46, SR>(z, bmax, alpha_c, sel, w, cd, e);
+          codes[h] = cd;
+          es[h] = e;
         }
-      }
-      if (col_ok) {
-        *reinterpret_cast<uint2*>(a.q_col + c * (M / 2) + r0 / 2) = make_uint2(lo, hi);
-        a.s_col[c * (M / 16) + r0 / 16] = (uint8_t)e;
+        tile::stage_col_pair(cstage, sstage, p, rb, codes[0], codes[1], es[0], es[1]);
       }
     }
+    __syncthreads();  // tile buffer free for the next prefetch; staging complete
+    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
   }
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR>
 cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
-  quant1d_kernel<ROW, COL, Q46, SR><<<tile_grid(a.M, a.N), kThreads, 0, s>>>(a);
+  constexpr bool kStash = SR && ROW && COL;
+  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + (kStash ? kStashBytes : 0);
+  auto kern = quant1d_kernel<ROW, COL, Q46, SR>;
+  // once per device: opt in to the dynamic shared memory and size the
+  // persistent grid from the occupancy
+  static int grid_cap[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int cap = (dev >= 0 && dev < 64) ? grid_cap[dev] : 0;
+  if (cap == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockThreads, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cap = (per_sm > 0 ? per_sm : 1) * sms;
+    if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
+  }
+  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
+  int64_t grid = ntiles < cap ? ntiles : cap;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kBlockThreads, kSmem, s>>>(a);
   return cudaGetLastError();
 }
 
