@@ -28,8 +28,30 @@ constexpr int kStatusNonFinite = -6;
 constexpr int kStatusRange = -7;
 
 // ---------------------------------------------------------------- bf16
+// Exact widening of the low / high bf16 half of a word by bit placement
+// (integer pipe).
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// The same widening as a mixed-precision add of -0.0 (exact, keeps the sign
+// of zero) so that it runs on the floating-point pipe, which has twice the
+// integer pipe's throughput.
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t v) {
+  float2 r;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, 0f80000000;\n"
+      " add.rn.f32.bf16 %1, h, 0f80000000;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(v));
+  return r;
+}
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
+  float2 r;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.f16 %0, l, 0f80000000;\n"
+      " add.rn.f32.f16 %1, h, 0f80000000;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(v));
+  return r;
+}
 
 // Packed FP32 pairs (Blackwell f32x2): two IEEE round-to-nearest operations
 // per instruction, each rounded exactly like its scalar counterpart.
@@ -200,6 +222,42 @@ __device__ __forceinline__ BlockScale block_scale(float b, float alpha, float Q)
   s.d = __fmul_rn(e4m3_value(s.e), alpha);
   s.inv = (s.d != 0.0f) ? __frcp_rn(s.d) : 0.0f;
   return s;
+}
+
+// Scale byte of a block: e = E4M3(fl(b / den)).  The quotient is taken as
+// b * (1/den), which is within 2 ulp of fl(b / den); the two give the same
+// E4M3 byte unless an E4M3 rounding midpoint (fp32 bits 19..0 == 0x80000 in
+// the normal range) lies within 3 ulp, or the value is in E4M3's subnormal
+// range -- then the IEEE division decides.  rden = 1/den, correctly rounded.
+__device__ __forceinline__ uint32_t scale_byte(float b, float den, float rden) {
+  if (!(b > 0.0f)) return 0u;
+  float t = __fmul_rn(b, rden);
+  const uint32_t low = __float_as_uint(t) & 0xFFFFFu;
+  if (low - 0x7FFFDu < 7u || t < 0x1p-6f) t = __fdiv_rn(b, den);
+  return e4m3_encode(t);
+}
+
+// Per-copy table of d = e*alpha and 1/d for every scale byte e (0..127),
+// filled once per CTA: entry e = (d, inv) exactly as block_scale computes them.
+__device__ __forceinline__ float2 scale_entry(uint32_t e, float alpha) {
+  const float d = __fmul_rn(e4m3_value(e), alpha);
+  return make_float2(d, (d != 0.0f) ? __frcp_rn(d) : 0.0f);
+}
+
+// Two values -> one code byte, plus the two codes' signed grid values as an
+// f16x2 (low half = first value).
+__device__ __forceinline__ uint32_t e2m1x2_enc_dec(float first, float second, uint32_t& h2) {
+  uint32_t byte;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n cvt.rn.f16x2.e2m1x2 %1, t;\n"
+      " cvt.u32.u8 %0, t;\n}"
+      : "=r"(byte), "=r"(h2)
+      : "f"(second), "f"(first));
+  return byte;
+}
+
+// Four bytes (low byte of each argument) -> one word, first argument lowest.
+__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
 // ---------------------------------------------------------------- 4/6 error terms

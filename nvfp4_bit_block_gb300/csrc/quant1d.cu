@@ -34,14 +34,28 @@ __device__ __forceinline__ int swz_stash(int q) { return q ^ ((q >> 3) & 7); }
 
 __device__ __forceinline__ uint2 ctr_of(uint64_t i) { return make_uint2((uint32_t)i, (uint32_t)(i >> 32)); }
 
-// Codes of 16 values at block scale s (block maximum Q), nibbles in element
-// order.  RN goes through the saturating cvt (a max-4 candidate whose scale
-// byte is subnormal is clamped to +-4 first, since |v| may then exceed 5);
-// SR rounds with the given Philox words.
+// Per-copy scale constants: den = Q*alpha and its correctly rounded
+// reciprocal for Q = 6 and Q = 4, and the shared (d, 1/d) table of alpha.
+struct CopyScales {
+  float den6, rden6, den4, rden4;
+  const float2* tbl;
+};
+
+__device__ __forceinline__ CopyScales make_scales(float alpha, const float2* tbl) {
+  CopyScales c;
+  c.den6 = __fmul_rn(6.0f, alpha);
+  c.den4 = __fmul_rn(4.0f, alpha);
+  c.rden6 = (c.den6 != 0.0f) ? __frcp_rn(c.den6) : 0.0f;
+  c.rden4 = (c.den4 != 0.0f) ? __frcp_rn(c.den4) : 0.0f;
+  c.tbl = tbl;
+  return c;
+}
+
+// v = z * inv for 16 values (packed), then SR rounding or, for a max-4
+// candidate with a subnormal scale byte, the clamp to +-4 that RN needs.
 template <bool SR>
-__device__ __forceinline__ uint2 codes16(const float* z, const BlockScale& s, float Q, const uint32_t* w) {
-  float v[16];
-  const float2 inv2 = make_float2(s.inv, s.inv);
+__device__ __forceinline__ void scale16(const float* z, float inv, uint32_t e, float Q, const uint32_t* w, float* v) {
+  const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
@@ -51,23 +65,21 @@ __device__ __forceinline__ uint2 codes16(const float* z, const BlockScale& s, fl
   if (SR) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = sr_round(v[j], Q, w[j]);
-  } else if (Q == 4.0f && s.e < 8u) {
+  } else if (Q == 4.0f && e < 8u) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
   }
-  return make_uint2(e2m1x8(v), e2m1x8(v + 8));
 }
 
-// 4/6 score of a 16-value block: err = z - val*d rounded once; MAE sums |err|,
-// MSE sums err*err, both over the perfect binary tree in block order;
-// MAXERR takes max |err|.
-__device__ __forceinline__ float score16(const float* z, uint2 codes, float d, int sel) {
+// 4/6 score of a 16-value block from the codes' decoded values h2 (f16x2
+// pairs): err = z - val*d rounded once; MAE sums |err|, MSE sums err*err,
+// both over the perfect binary tree in block order; MAXERR takes max |err|.
+__device__ __forceinline__ float score16(const float* z, const uint32_t* h2, float d, int sel) {
   const float2 nd = make_float2(-d, -d);
   float e[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint32_t word = (j < 4) ? codes.x : codes.y;
-    const float2 val = e2m1x2_values((word >> (8 * (j & 3))) & 0xFFu);
+    const float2 val = f16x2_to_f32x2(h2[j]);
     const float2 err = fma2(val, nd, make_float2(z[2 * j], z[2 * j + 1]));
     e[2 * j] = err.x;
     e[2 * j + 1] = err.y;
@@ -99,29 +111,76 @@ __device__ __forceinline__ float score16(const float* z, uint2 codes, float d, i
 // One block: the standard max-6 candidate and, with 4/6, the max-4 candidate;
 // the max-4 one is kept only if its score is strictly lower.
 template <bool Q46, bool SR>
-__device__ __forceinline__ void quant_block16(const float* z, float bmax, float alpha, int sel,
+__device__ __forceinline__ void quant_block16(const float* z, float bmax, const CopyScales& sc, int sel,
                                               const uint32_t* w, uint2& codes, uint32_t& e) {
-  const BlockScale s6 = block_scale(bmax, alpha, 6.0f);
-  codes = codes16<SR>(z, s6, 6.0f, w);
-  e = s6.e;
-  if (Q46) {
-    const BlockScale s4 = block_scale(bmax, alpha, 4.0f);
-    const uint2 c4 = codes16<SR>(z, s4, 4.0f, w);
-    if (score16(z, c4, s4.d, sel) < score16(z, codes, s6.d, sel)) {
-      codes = c4;
-      e = s4.e;
-    }
+  const uint32_t e6 = scale_byte(bmax, sc.den6, sc.rden6);
+  const float2 di6 = sc.tbl[e6];
+  float v[16];
+  scale16<SR>(z, di6.y, e6, 6.0f, w, v);
+  if (!Q46) {
+    codes = make_uint2(e2m1x8(v), e2m1x8(v + 8));
+    e = e6;
+    return;
+  }
+  const uint32_t e4 = scale_byte(bmax, sc.den4, sc.rden4);
+  const float2 di4 = sc.tbl[e4];
+  uint32_t b6[8], h6[8], b4[8], h4[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b6[j] = e2m1x2_enc_dec(v[2 * j], v[2 * j + 1], h6[j]);
+  scale16<SR>(z, di4.y, e4, 4.0f, w, v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b4[j] = e2m1x2_enc_dec(v[2 * j], v[2 * j + 1], h4[j]);
+  if (score16(z, h4, di4.x, sel) < score16(z, h6, di6.x, sel)) {
+    codes = make_uint2(pack4(b4[0], b4[1], b4[2], b4[3]), pack4(b4[4], b4[5], b4[6], b4[7]));
+    e = e4;
+  } else {
+    codes = make_uint2(pack4(b6[0], b6[1], b6[2], b6[3]), pack4(b6[4], b6[5], b6[6], b6[7]));
+    e = e6;
+  }
+}
+
+// Per-thread tile loader: thread `tid` copies chunks (row tid/32 + 8k, chunk
+// tid%32) for k = 0..7; the global and shared offsets are fixed per thread.
+struct Loader {
+  int64_t goff;  // (tid/32)*ld + 8*(tid%32)
+  int64_t ld8;   // 8*ld
+  uint32_t soff; // shared offset of k = 0
+  int lr, lc;    // tid/32, tid%32
+};
+
+__device__ __forceinline__ Loader make_loader(int tid, int64_t ld) {
+  Loader L;
+  L.lr = tid >> 5;
+  L.lc = tid & 31;
+  L.goff = (int64_t)L.lr * ld + 8 * L.lc;
+  L.ld8 = 8 * ld;
+  L.soff = L.lr * tile::kRowBytes + tile::swz(L.lc) * 16;
+  return L;
+}
+
+__device__ __forceinline__ void load_tile(uint8_t* buf, const QuantArgs& a, const Loader& L, int64_t R0, int64_t C0) {
+  const uint16_t* base = a.x + R0 * a.ld + C0 + L.goff;
+  const bool full = (R0 + kTM <= a.M) && (C0 + kTN <= a.N);
+  const uint32_t dst0 = tile::smem_u32(buf) + L.soff;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const bool ok = full || ((R0 + L.lr + 8 * k < a.M) && (C0 + 8 * L.lc < a.N));
+    const uint16_t* src = ok ? base + k * L.ld8 : a.x;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
   }
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR>
-__global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kBlockThreads, (Q46 || SR) ? 2 : 3) quant1d_kernel(const QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr bool kStash = SR && ROW && COL;
   uint8_t* bufs = smem;                                      // 2 x 32 KB tiles
   uint8_t* cstage = smem + 2 * tile::kTileBytes;             // 8 KB
   uint8_t* sstage = cstage + tile::kCStageBytes;             // 1 KB
-  uint8_t* stash = sstage + tile::kSStageBytes;              // 64 KB with kStash
+  float2* tbl = reinterpret_cast<float2*>(sstage + tile::kSStageBytes);  // 2 x 128 (d, 1/d)
+  uint8_t* stash = reinterpret_cast<uint8_t*>(tbl + 256);    // 64 KB with kStash
 
   // a2: alpha = amax / (6*448), or amax / (6*256) with 4/6
   const float den = Q46 ? kAlphaDen46 : kAlphaDen;
@@ -130,7 +189,7 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
   const float alpha_c = __fdiv_rn(A_c, den);
   const int st_r = ROW ? amax_status(A_r) : 0;
   const int st_c = COL ? amax_status(A_c) : 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     a.alpha[0] = alpha_r;
     a.alpha[1] = alpha_c;
     if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
@@ -138,41 +197,48 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
   if (st_r || st_c) return;
 
   const int64_t M = a.M, N = a.N;
-  const int64_t ntx = (N + kTN - 1) / kTN;
-  const int64_t ntiles = ((M + kTM - 1) / kTM) * ntx;
+  const int64_t nty = (M + kTM - 1) / kTM;
+  const int64_t C0 = (int64_t)blockIdx.x * kTN;
   const int tid = threadIdx.x;
+  tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);  // read after the first barrier
+  const CopyScales scR = make_scales(alpha_r, tbl);
+  const CopyScales scC = make_scales(alpha_c, tbl + 128);
   const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
   const int sel = a.sel;
+  const Loader L = make_loader(tid, a.ld);
+  // fixed task coordinates of this thread
+  const int rb_b = tid & 15, rb_r0 = tid >> 4;   // rowwise: block column, first row
+  const int cp_p = tid & 127, cp_rb0 = tid >> 7; // columnwise: column pair, first row block
 
-  int64_t t = blockIdx.x;
-  if (t < ntiles) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, tile::coord(t, ntx), tid);
+  int64_t ty = blockIdx.y;
+  if (ty < nty) load_tile(bufs, a, L, ty * kTM, C0);
   tile::commit();
-  for (int it = 0; t < ntiles; t += gridDim.x, ++it) {
+  for (int it = 0; ty < nty; ty += gridDim.y, ++it) {
     uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
-    const int64_t tn = t + gridDim.x;
-    if (tn < ntiles)  // prefetch the next tile into the other buffer
-      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld,
-                                      tile::coord(tn, ntx), tid);
+    const int64_t tn = ty + gridDim.y;
+    if (tn < nty) load_tile(bufs + ((it + 1) & 1) * tile::kTileBytes, a, L, tn * kTM, C0);
     tile::commit();
     tile::wait_all_but_one();
     __syncthreads();
-    const tile::Coord tc = tile::coord(t, ntx);
+    const int64_t R0 = ty * kTM;
+    const tile::Coord tc = {R0, C0};
 
     // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
     if (ROW) {
+      const int64_t gcol = C0 + 16 * rb_b;
 #pragma unroll 1
-      for (int k = 0; k < kTM * 16 / kBlockThreads; ++k) {
-        const int task = tid + k * kBlockThreads;
-        const int r = task >> 4, b = task & 15;
-        const int64_t grow = tc.R0 + r, gcol = tc.C0 + 16 * b;
+      for (int k = 0; k < 4; ++k) {
+        const int r = rb_r0 + 16 * k;
+        const int64_t grow = R0 + r;
         if (grow >= M || gcol >= N) continue;
         uint32_t wd[8];
-        tile::read_row_block(buf, r, b, wd);
+        tile::read_row_block(buf, r, rb_b, wd);
         float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          z[2 * j] = bf16_lo(wd[j]);
-          z[2 * j + 1] = bf16_hi(wd[j]);
+          const float2 f = bf16x2_to_f32x2(wd[j]);
+          z[2 * j] = f.x;
+          z[2 * j + 1] = f.y;
         }
         float bmax;
         if (a.rht_row) {
@@ -198,13 +264,13 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
             uint8_t* srow = stash + r * (kTN * 4);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(srow + swz_stash(4 * b + q) * 16) =
+              *reinterpret_cast<uint4*>(srow + swz_stash(4 * rb_b + q) * 16) =
                   make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
           }
         }
         uint2 codes;
         uint32_t e;
-        quant_block16<Q46, SR>(z, bmax, alpha_r, sel, w, codes, e);
+        quant_block16<Q46, SR>(z, bmax, scR, sel, w, codes, e);
         *reinterpret_cast<uint2*>(a.q_row + grow * (N / 2) + gcol / 2) = codes;
         a.s_row[grow * (N / 16) + gcol / 16] = (uint8_t)e;
       }
@@ -213,11 +279,12 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
 
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
     if (COL) {
+      const int p = cp_p;
+      const int64_t gcol = C0 + 2 * p;
 #pragma unroll 1
-      for (int k = 0; k < (kTN / 2) * (kTM / 16) / kBlockThreads; ++k) {
-        const int task = tid + k * kBlockThreads;
-        const int p = task & 127, rb = task >> 7;
-        const int64_t gcol = tc.C0 + 2 * p, grow0 = tc.R0 + 16 * rb;
+      for (int k = 0; k < 2; ++k) {
+        const int rb = cp_rb0 + 2 * k;
+        const int64_t grow0 = R0 + 16 * rb;
         if (gcol >= N || grow0 >= M) continue;
         uint32_t wd[16];
 #pragma unroll
@@ -234,11 +301,16 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
         }
         uint2 codes[2];
         uint32_t es[2];
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float z[16];
+        float zz[2][16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) z[i] = h ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = bf16x2_to_f32x2(wd[i]);
+          zz[0][i] = f.x;
+          zz[1][i] = f.y;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float* z = zz[h];
           float bmax = h ? bf16_hi(m2) : bf16_lo(m2);
           if (a.rht_col) {
             rht16(z, signs);
@@ -264,7 +336,7 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
           }
           uint2 cd;
           uint32_t e;
-          quant_block16<Q46, SR>(z, bmax, alpha_c, sel, w, cd, e);
+          quant_block16<Q46, SR>(z, bmax, scC, sel, w, cd, e);
           codes[h] = cd;
           es[h] = e;
         }
@@ -279,7 +351,8 @@ __global__ void __launch_bounds__(kBlockThreads) quant1d_kernel(const QuantArgs 
 template <bool ROW, bool COL, bool Q46, bool SR>
 cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   constexpr bool kStash = SR && ROW && COL;
-  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + (kStash ? kStashBytes : 0);
+  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
+                        (kStash ? kStashBytes : 0);
   auto kern = quant1d_kernel<ROW, COL, Q46, SR>;
   // once per device: opt in to the dynamic shared memory and size the
   // persistent grid from the occupancy
@@ -298,10 +371,14 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
     cap = (per_sm > 0 ? per_sm : 1) * sms;
     if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
   }
-  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
-  int64_t grid = ntiles < cap ? ntiles : cap;
-  if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kBlockThreads, kSmem, s>>>(a);
+  // columns of tiles across x; each CTA walks a strided set of row tiles
+  const int64_t ntx = (a.N + kTN - 1) / kTN, nty = (a.M + kTM - 1) / kTM;
+  int64_t gy = ntx > 0 ? cap / ntx : 1;
+  if (gy > nty) gy = nty;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  const dim3 grid((unsigned)(ntx > 0 ? ntx : 1), (unsigned)gy, 1);
+  kern<<<grid, kBlockThreads, kSmem, s>>>(a);
   return cudaGetLastError();
 }
 
