@@ -114,7 +114,7 @@ def run_ours(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     nv.lib()
-    flags, sel = synthetic.workload_flags(args.workload)
+    flags, sel = workload_config(args)
     bits = synthetic.workload(args.workload)
     M, N = bits.shape
     x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -243,11 +243,39 @@ def run_ours(args, rank: int, world: int):
     return res
 
 
+def workload_config(args):
+    flags, sel = synthetic.workload_flags(args.workload)
+    if getattr(args, "flags", None) is not None:
+        flags = args.flags
+    if getattr(args, "sel", None) is not None:
+        sel = args.sel
+    return flags, sel
+
+
+def run_once(args):
+    """Three amax + quantize passes on one workload, nothing timed: the
+    command the ncu captures under profiles/ run."""
+    import torch
+
+    import nvfp4_bit_block_gb300 as nv
+
+    nv.lib()
+    flags, sel = workload_config(args)
+    bits = synthetic.workload(args.workload)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    for _ in range(3):
+        amax = nv.nvfp4_amax(x, flags, synthetic.RHT_SEED)
+        out = nv.nvfp4_quantize(x, amax, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED)
+    torch.cuda.synchronize()
+    assert int(out.status.item()) == 0
+    print(json.dumps({"once": args.workload, "flags": flags, "selection": sel}))
+
+
 def run_oracle_sample(args, max_seconds: float = 20.0):
     """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
     import oracle
 
-    flags, sel = synthetic.workload_flags(args.workload)
+    flags, sel = workload_config(args)
     bits = synthetic.workload(args.workload)
     M, N = bits.shape
     t0 = time.perf_counter()
@@ -281,7 +309,14 @@ def main():
     ap.add_argument("--workload", default="act_46mae_8192x5120", choices=list(synthetic.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flags", type=int, default=None, help="override the workload's flags")
+    ap.add_argument("--sel", type=int, default=None, help="override the workload's 4/6 selection rule")
+    ap.add_argument("--once", action="store_true",
+                    help="run amax + quantize three times on the workload and exit (for profilers)")
     args = ap.parse_args()
+    if args.once:
+        run_once(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
 
@@ -294,7 +329,7 @@ def main():
             cb = run_oracle_sample(args, max_seconds=4.0)
             per_step.append(cb["value"])
         v = statistics.mean(per_step[args.warmup:]) if args.steps else per_step[-1]
-        flags, sel = synthetic.workload_flags(args.workload)
+        flags, sel = workload_config(args)
         _, M, N = synthetic.WORKLOADS[args.workload][:3]
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,

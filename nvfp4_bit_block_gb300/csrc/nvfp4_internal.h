@@ -42,6 +42,9 @@ struct DequantArgs {
 
 cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
+cudaError_t launch_quant1d_46_mae(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
+cudaError_t launch_quant1d_46_mse(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
+cudaError_t launch_quant1d_46_max(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
 cudaError_t launch_quant2d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 

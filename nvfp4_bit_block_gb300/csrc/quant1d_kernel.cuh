@@ -1,0 +1,402 @@
+#pragma once
+// quant1d_kernel.cuh -- fused rowwise + columnwise NVFP4 quantization with 1x16 blocks.
+//
+// One read of X produces both copies.  Persistent CTAs stream 64 x 256 bf16
+// tiles through double-buffered shared memory (tile_pipeline.cuh), then
+//   - the rowwise pass gives each thread whole 16-column blocks (two 128-bit
+//     shared loads) and stores their codes directly (coalesced), and
+//   - the columnwise pass gives each thread a column pair over 16 rows (sixteen
+//     32-bit shared loads, one bf16x2 word per row) and stages the codes, so
+//     that each column of the transposed copy is written as one 32-byte store,
+// so every block's scale, rounding and 4/6 choice happen in one thread's
+// registers.  Element arithmetic uses packed f32x2 operations, which halve
+// the issue slots of the multiplies and fused multiply-adds.
+//
+// With stochastic rounding on both copies, one Philox4x32-10 call per element
+// serves both: the rowwise pass uses word 0 and parks word 1 in shared memory
+// for the columnwise pass.
+//
+// Sources: "Four Over Six (4/6)" technical summary (Problem statement,
+// Methodology, Implementation details) and "Pretraining Large Language Models
+// with NVFP4" sections 1, 2b and 2d.
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+#include "tile_pipeline.cuh"
+
+#ifndef NVFP4_Q1D_MIN_CTAS
+#define NVFP4_Q1D_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for
+#endif
+
+namespace nvfp4 {
+namespace q1d {
+
+using tile::kTM;
+using tile::kTN;
+constexpr int kStashBytes = kTM * kTN * 4;  // Philox word 1 per element, 64 KB
+constexpr int kBlockThreads = 256;
+
+// 16-byte chunk q of a stash row (64 chunks) lives at chunk q ^ ((q >> 3) & 7)
+__device__ __forceinline__ int swz_stash(int q) { return q ^ ((q >> 3) & 7); }
+
+__device__ __forceinline__ uint2 ctr_of(uint64_t i) { return make_uint2((uint32_t)i, (uint32_t)(i >> 32)); }
+
+// Per-copy scale constants: den = Q*alpha and its correctly rounded
+// reciprocal for Q = 6 and Q = 4, and the shared (d, 1/d) table of alpha.
+struct CopyScales {
+  float den6, rden6, den4, rden4;
+  const float2* tbl;
+};
+
+__device__ __forceinline__ CopyScales make_scales(float alpha, const float2* tbl) {
+  CopyScales c;
+  c.den6 = __fmul_rn(6.0f, alpha);
+  c.den4 = __fmul_rn(4.0f, alpha);
+  c.rden6 = (c.den6 != 0.0f) ? __frcp_rn(c.den6) : 0.0f;
+  c.rden4 = (c.den4 != 0.0f) ? __frcp_rn(c.den4) : 0.0f;
+  c.tbl = tbl;
+  return c;
+}
+
+// v = z * inv for 16 values (packed), then SR rounding or, for a max-4
+// candidate with a subnormal scale byte, the clamp to +-4 that RN needs.
+template <bool SR>
+__device__ __forceinline__ void scale16(const float* z, float inv, uint32_t e, float Q, const uint32_t* w, float* v) {
+  const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
+    v[2 * j] = r.x;
+    v[2 * j + 1] = r.y;
+  }
+  if (SR) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = sr_round(v[j], Q, w[j]);
+  } else if (Q == 4.0f && e < 8u) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
+  }
+}
+
+// Codes of one 4/6 candidate and its score, computed pair by pair so that
+// only the code bytes and eight partial sums stay live: for each pair the
+// scaled values are encoded, the codes decoded back to grid values, and
+// err = z - val*d (rounded once) folded into the first level of the tree.
+// MAE sums |err|, MSE sums err*err, both over the perfect binary tree in
+// block order; MAXERR takes max |err|.
+template <bool SR, int SEL>
+__device__ __forceinline__ float candidate16(const float* z, uint32_t e, float2 di, float Q, const uint32_t* w,
+                                             uint32_t* bytes) {
+  const float2 inv2 = make_float2(di.y, di.y);
+  const float2 nd = make_float2(-di.x, -di.x);
+  const bool clamp = !SR && Q == 4.0f && e < 8u;
+  float t[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 zz = make_float2(z[2 * j], z[2 * j + 1]);
+    float2 v = mul2(zz, inv2);
+    if (SR) {
+      v.x = sr_round(v.x, Q, w[2 * j]);
+      v.y = sr_round(v.y, Q, w[2 * j + 1]);
+    } else if (clamp) {
+      v.x = fminf(fmaxf(v.x, -4.0f), 4.0f);
+      v.y = fminf(fmaxf(v.y, -4.0f), 4.0f);
+    }
+    uint32_t h2;
+    bytes[j] = e2m1x2_enc_dec(v.x, v.y, h2);
+    const float2 err = fma2(f16x2_to_f32x2(h2), nd, zz);  // z - val*d, rounded once
+    if (SEL == kSelMSE) {
+      const float2 sq = mul2(err, err);
+      t[j] = __fadd_rn(sq.x, sq.y);
+    } else if (SEL == kSelMax) {
+      t[j] = fmaxf(fabsf(err.x), fabsf(err.y));
+    } else {
+      t[j] = __fadd_rn(fabsf(err.x), fabsf(err.y));
+    }
+  }
+  if (SEL == kSelMax)
+    return fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
+  // ((t0+t1)+(t2+t3)) + ((t4+t5)+(t6+t7)), two sums per packed add
+  const float2 a = add2(make_float2(t[0], t[4]), make_float2(t[1], t[5]));
+  const float2 b = add2(make_float2(t[2], t[6]), make_float2(t[3], t[7]));
+  const float2 c = add2(a, b);
+  return __fadd_rn(c.x, c.y);
+}
+
+// One block: the standard max-6 candidate and, with 4/6, the max-4 candidate;
+// the max-4 one is kept only if its score is strictly lower.
+template <bool Q46, bool SR, int SEL>
+__device__ __forceinline__ void quant_block16(const float* z, float bmax, const CopyScales& sc, const uint32_t* w,
+                                              uint2& codes, uint32_t& e) {
+  const uint32_t e6 = scale_byte(bmax, sc.den6, sc.rden6);
+  const float2 di6 = sc.tbl[e6];
+  if (!Q46) {
+    float v[16];
+    scale16<SR>(z, di6.y, e6, 6.0f, w, v);
+    codes = make_uint2(e2m1x8(v), e2m1x8(v + 8));
+    e = e6;
+    return;
+  }
+  uint32_t b6[8], b4[8];
+  const float s6 = candidate16<SR, SEL>(z, e6, di6, 6.0f, w, b6);
+  const uint32_t e4 = scale_byte(bmax, sc.den4, sc.rden4);
+  const float s4 = candidate16<SR, SEL>(z, e4, sc.tbl[e4], 4.0f, w, b4);
+  const bool four = s4 < s6;
+  uint32_t b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = four ? b4[j] : b6[j];
+  codes = make_uint2(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]));
+  e = four ? e4 : e6;
+}
+
+// Per-thread tile loader: thread `tid` copies chunks (row tid/32 + 8k, chunk
+// tid%32) for k = 0..7; the global and shared offsets are fixed per thread.
+struct Loader {
+  int64_t goff;  // (tid/32)*ld + 8*(tid%32)
+  int64_t ld8;   // 8*ld
+  uint32_t soff; // shared offset of k = 0
+  int lr, lc;    // tid/32, tid%32
+};
+
+__device__ __forceinline__ Loader make_loader(int tid, int64_t ld) {
+  Loader L;
+  L.lr = tid >> 5;
+  L.lc = tid & 31;
+  L.goff = (int64_t)L.lr * ld + 8 * L.lc;
+  L.ld8 = 8 * ld;
+  L.soff = L.lr * tile::kRowBytes + tile::swz(L.lc) * 16;
+  return L;
+}
+
+__device__ __forceinline__ void load_tile(uint8_t* buf, const QuantArgs& a, const Loader& L, int64_t R0, int64_t C0) {
+  const uint16_t* base = a.x + R0 * a.ld + C0 + L.goff;
+  const bool full = (R0 + kTM <= a.M) && (C0 + kTN <= a.N);
+  const uint32_t dst0 = tile::smem_u32(buf) + L.soff;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const bool ok = full || ((R0 + L.lr + 8 * k < a.M) && (C0 + 8 * L.lc < a.N));
+    const uint16_t* src = ok ? base + k * L.ld8 : a.x;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+  }
+}
+
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
+__global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) quant1d_kernel(const QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr bool kStash = SR && ROW && COL;
+  uint8_t* bufs = smem;                                      // 2 x 32 KB tiles
+  uint8_t* cstage = smem + 2 * tile::kTileBytes;             // 8 KB
+  uint8_t* sstage = cstage + tile::kCStageBytes;             // 1 KB
+  float2* tbl = reinterpret_cast<float2*>(sstage + tile::kSStageBytes);  // 2 x 128 (d, 1/d)
+  uint8_t* stash = reinterpret_cast<uint8_t*>(tbl + 256);    // 64 KB with kStash
+
+  // a2: alpha = amax / (6*448), or amax / (6*256) with 4/6
+  const float den = Q46 ? kAlphaDen46 : kAlphaDen;
+  const float A_r = a.amax[0], A_c = a.amax[1];
+  const float alpha_r = __fdiv_rn(A_r, den);
+  const float alpha_c = __fdiv_rn(A_c, den);
+  const int st_r = ROW ? amax_status(A_r) : 0;
+  const int st_c = COL ? amax_status(A_c) : 0;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    a.alpha[0] = alpha_r;
+    a.alpha[1] = alpha_c;
+    if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
+  }
+  if (st_r || st_c) return;
+
+  const int64_t M = a.M, N = a.N;
+  const int64_t nty = (M + kTM - 1) / kTM;
+  const int64_t C0 = (int64_t)blockIdx.x * kTN;
+  const int tid = threadIdx.x;
+  tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);  // read after the first barrier
+  const CopyScales scR = make_scales(alpha_r, tbl);
+  const CopyScales scC = make_scales(alpha_c, tbl + 128);
+  const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
+  const Loader L = make_loader(tid, a.ld);
+  // fixed task coordinates of this thread
+  const int rb_b = tid & 15, rb_r0 = tid >> 4;   // rowwise: block column, first row
+  const int cp_p = tid & 127, cp_rb0 = tid >> 7; // columnwise: column pair, first row block
+
+  int64_t ty = blockIdx.y;
+  if (ty < nty) load_tile(bufs, a, L, ty * kTM, C0);
+  tile::commit();
+  for (int it = 0; ty < nty; ty += gridDim.y, ++it) {
+    uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
+    const int64_t tn = ty + gridDim.y;
+    if (tn < nty) load_tile(bufs + ((it + 1) & 1) * tile::kTileBytes, a, L, tn * kTM, C0);
+    tile::commit();
+    tile::wait_all_but_one();
+    __syncthreads();
+    const int64_t R0 = ty * kTM;
+    const tile::Coord tc = {R0, C0};
+
+    // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
+    if (ROW) {
+      const int64_t gcol = C0 + 16 * rb_b;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        const int r = rb_r0 + 16 * k;
+        const int64_t grow = R0 + r;
+        if (grow >= M || gcol >= N) continue;
+        uint32_t wd[8];
+        tile::read_row_block(buf, r, rb_b, wd);
+        float z[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = bf16x2_to_f32x2(wd[j]);
+          z[2 * j] = f.x;
+          z[2 * j + 1] = f.y;
+        }
+        float bmax;
+        if (a.rht_row) {
+          rht16(z, signs);
+          bmax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(z[j]));
+        } else {
+          bmax = block_absmax16(wd);
+        }
+        uint32_t w[16];
+        if (SR) {
+          const uint64_t base = a.ctr_off + (uint64_t)grow * (uint64_t)N + (uint64_t)gcol;
+          uint32_t w1[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint2 c = ctr_of(base + j);
+            const uint2 pw = philox_w01(c.x, c.y, a.sr_k0, a.sr_k1);
+            w[j] = pw.x;
+            w1[j] = pw.y;
+          }
+          if (kStash) {
+            uint8_t* srow = stash + r * (kTN * 4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(srow + swz_stash(4 * rb_b + q) * 16) =
+                  make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+          }
+        }
+        uint2 codes;
+        uint32_t e;
+        quant_block16<Q46, SR, SEL>(z, bmax, scR, w, codes, e);
+        *reinterpret_cast<uint2*>(a.q_row + grow * (N / 2) + gcol / 2) = codes;
+        a.s_row[grow * (N / 16) + gcol / 16] = (uint8_t)e;
+      }
+    }
+    if (kStash) __syncthreads();
+
+    // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
+    if (COL) {
+      const int p = cp_p;
+      const int64_t gcol = C0 + 2 * p;
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        const int rb = cp_rb0 + 2 * k;
+        const int64_t grow0 = R0 + 16 * rb;
+        if (gcol >= N || grow0 >= M) continue;
+        uint32_t wd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, p);
+        // both columns' maxima at once (low half = column 2p, high half = 2p+1)
+        uint32_t m2 = 0u;
+        if (!a.rht_col) {
+          uint32_t t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(wd[2 * i], wd[2 * i + 1]);
+          m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(t8[0], t8[1]), absmax_bf16x2(t8[2], t8[3])),
+                             absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7]))) &
+               0x7FFF7FFFu;
+        }
+        uint2 codes[2];
+        uint32_t es[2];
+        float zz[2][16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = bf16x2_to_f32x2(wd[i]);
+          zz[0][i] = f.x;
+          zz[1][i] = f.y;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float* z = zz[h];
+          float bmax = h ? bf16_hi(m2) : bf16_lo(m2);
+          if (a.rht_col) {
+            rht16(z, signs);
+            bmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(z[i]));
+          }
+          const int cc = 2 * p + h;  // tile column
+          uint32_t w[16];
+          if (SR) {
+            if (kStash) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = *reinterpret_cast<const uint32_t*>(stash + (16 * rb + i) * (kTN * 4) +
+                                                          swz_stash(cc >> 2) * 16 + (cc & 3) * 4);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const uint2 ct = ctr_of(a.ctr_off + (uint64_t)(grow0 + i) * (uint64_t)N + (uint64_t)(gcol + h));
+                w[i] = philox_w01(ct.x, ct.y, a.sr_k0, a.sr_k1).y;
+              }
+            }
+          }
+          uint2 cd;
+          uint32_t e;
+          quant_block16<Q46, SR, SEL>(z, bmax, scC, w, cd, e);
+          codes[h] = cd;
+          es[h] = e;
+        }
+        tile::stage_col_pair(cstage, sstage, p, rb, codes[0], codes[1], es[0], es[1]);
+      }
+    }
+    __syncthreads();  // tile buffer free for the next prefetch; staging complete
+    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
+  }
+}
+
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
+cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
+  constexpr bool kStash = SR && ROW && COL;
+  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
+                        (kStash ? kStashBytes : 0);
+  auto kern = quant1d_kernel<ROW, COL, Q46, SR, SEL>;
+  // once per device: opt in to the dynamic shared memory and size the
+  // persistent grid from the occupancy
+  static int grid_cap[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int cap = (dev >= 0 && dev < 64) ? grid_cap[dev] : 0;
+  if (cap == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockThreads, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cap = (per_sm > 0 ? per_sm : 1) * sms;
+    if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
+  }
+  // columns of tiles across x; each CTA walks a strided set of row tiles
+  const int64_t ntx = (a.N + kTN - 1) / kTN, nty = (a.M + kTM - 1) / kTM;
+  int64_t gy = ntx > 0 ? cap / ntx : 1;
+  if (gy > nty) gy = nty;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  const dim3 grid((unsigned)(ntx > 0 ? ntx : 1), (unsigned)gy, 1);
+  kern<<<grid, kBlockThreads, kSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// All row/column/SR combinations of one (4/6, selection rule) pair.
+template <bool Q46, int SEL>
+cudaError_t launch_family(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s) {
+  if (row && col) return sr ? launch<true, true, Q46, true, SEL>(a, s) : launch<true, true, Q46, false, SEL>(a, s);
+  if (row) return sr ? launch<true, false, Q46, true, SEL>(a, s) : launch<true, false, Q46, false, SEL>(a, s);
+  return sr ? launch<false, true, Q46, true, SEL>(a, s) : launch<false, true, Q46, false, SEL>(a, s);
+}
+
+}  // namespace q1d
+}  // namespace nvfp4
