@@ -255,6 +255,25 @@ __device__ __forceinline__ uint32_t e2m1x2_enc_dec(float first, float second, ui
   return byte;
 }
 
+// Eight values -> eight nibbles (value j in bits 4j..4j+3), plus the codes'
+// signed grid values as four f16x2 words (h[k] holds values 2k, 2k+1).
+__device__ __forceinline__ uint32_t e2m1x8_enc_dec(const float* v, uint32_t* h) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %8, %7;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %10, %9;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %12, %11;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 %4, b3;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // Four bytes (low byte of each argument) -> one word, first argument lowest.
 __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);

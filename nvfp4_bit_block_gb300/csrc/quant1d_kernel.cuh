@@ -85,34 +85,47 @@ __device__ __forceinline__ void scale16(const float* z, float inv, uint32_t e, f
 // block order; MAXERR takes max |err|.
 template <bool SR, int SEL>
 __device__ __forceinline__ float candidate16(const float* z, uint32_t e, float2 di, float Q, const uint32_t* w,
-                                             uint32_t* bytes) {
+                                             uint2& codes) {
   const float2 inv2 = make_float2(di.y, di.y);
   const float2 nd = make_float2(-di.x, -di.x);
   const bool clamp = !SR && Q == 4.0f && e < 8u;
   float t[8];
+  uint32_t cw[2];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float2 zz = make_float2(z[2 * j], z[2 * j + 1]);
-    float2 v = mul2(zz, inv2);
-    if (SR) {
-      v.x = sr_round(v.x, Q, w[2 * j]);
-      v.y = sr_round(v.y, Q, w[2 * j + 1]);
-    } else if (clamp) {
-      v.x = fminf(fmaxf(v.x, -4.0f), 4.0f);
-      v.y = fminf(fmaxf(v.y, -4.0f), 4.0f);
+  for (int half = 0; half < 2; ++half) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 r = mul2(make_float2(z[8 * half + 2 * j], z[8 * half + 2 * j + 1]), inv2);
+      v[2 * j] = r.x;
+      v[2 * j + 1] = r.y;
     }
-    uint32_t h2;
-    bytes[j] = e2m1x2_enc_dec(v.x, v.y, h2);
-    const float2 err = fma2(f16x2_to_f32x2(h2), nd, zz);  // z - val*d, rounded once
-    if (SEL == kSelMSE) {
-      const float2 sq = mul2(err, err);
-      t[j] = __fadd_rn(sq.x, sq.y);
-    } else if (SEL == kSelMax) {
-      t[j] = fmaxf(fabsf(err.x), fabsf(err.y));
-    } else {
-      t[j] = __fadd_rn(fabsf(err.x), fabsf(err.y));
+    if (SR) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = sr_round(v[j], Q, w[8 * half + j]);
+    } else if (clamp) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
+    }
+    uint32_t h2[4];
+    cw[half] = e2m1x8_enc_dec(v, h2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 zz = make_float2(z[8 * half + 2 * j], z[8 * half + 2 * j + 1]);
+      const float2 err = fma2(f16x2_to_f32x2(h2[j]), nd, zz);  // z - val*d, rounded once
+      float tj;
+      if (SEL == kSelMSE) {
+        const float2 sq = mul2(err, err);
+        tj = __fadd_rn(sq.x, sq.y);
+      } else if (SEL == kSelMax) {
+        tj = fmaxf(fabsf(err.x), fabsf(err.y));
+      } else {
+        tj = __fadd_rn(fabsf(err.x), fabsf(err.y));
+      }
+      t[4 * half + j] = tj;
     }
   }
+  codes = make_uint2(cw[0], cw[1]);
   if (SEL == kSelMax)
     return fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
   // ((t0+t1)+(t2+t3)) + ((t4+t5)+(t6+t7)), two sums per packed add
@@ -136,15 +149,12 @@ __device__ __forceinline__ void quant_block16(const float* z, float bmax, const 
     e = e6;
     return;
   }
-  uint32_t b6[8], b4[8];
-  const float s6 = candidate16<SR, SEL>(z, e6, di6, 6.0f, w, b6);
+  uint2 c6, c4;
+  const float s6 = candidate16<SR, SEL>(z, e6, di6, 6.0f, w, c6);
   const uint32_t e4 = scale_byte(bmax, sc.den4, sc.rden4);
-  const float s4 = candidate16<SR, SEL>(z, e4, sc.tbl[e4], 4.0f, w, b4);
+  const float s4 = candidate16<SR, SEL>(z, e4, sc.tbl[e4], 4.0f, w, c4);
   const bool four = s4 < s6;
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = four ? b4[j] : b6[j];
-  codes = make_uint2(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]));
+  codes = four ? c4 : c6;
   e = four ? e4 : e6;
 }
 
