@@ -1,7 +1,7 @@
 // api.cu -- the C ABI declared in include/nvfp4.h: host-side argument
 // validation, flag decoding and kernel dispatch.  Nothing here allocates
 // memory or keeps state; every call enqueues work on the caller's stream.
-#include "../../include/nvfp4.h"
+#include "nvfp4.h"
 
 #include <cuda_runtime.h>
 

@@ -158,39 +158,6 @@ __device__ __forceinline__ void quant_block16(const float* z, float bmax, const 
   e = four ? e4 : e6;
 }
 
-// Per-thread tile loader: thread `tid` copies chunks (row tid/32 + 8k, chunk
-// tid%32) for k = 0..7; the global and shared offsets are fixed per thread.
-struct Loader {
-  int64_t goff;  // (tid/32)*ld + 8*(tid%32)
-  int64_t ld8;   // 8*ld
-  uint32_t soff; // shared offset of k = 0
-  int lr, lc;    // tid/32, tid%32
-};
-
-__device__ __forceinline__ Loader make_loader(int tid, int64_t ld) {
-  Loader L;
-  L.lr = tid >> 5;
-  L.lc = tid & 31;
-  L.goff = (int64_t)L.lr * ld + 8 * L.lc;
-  L.ld8 = 8 * ld;
-  L.soff = L.lr * tile::kRowBytes + tile::swz(L.lc) * 16;
-  return L;
-}
-
-__device__ __forceinline__ void load_tile(uint8_t* buf, const QuantArgs& a, const Loader& L, int64_t R0, int64_t C0) {
-  const uint16_t* base = a.x + R0 * a.ld + C0 + L.goff;
-  const bool full = (R0 + kTM <= a.M) && (C0 + kTN <= a.N);
-  const uint32_t dst0 = tile::smem_u32(buf) + L.soff;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const bool ok = full || ((R0 + L.lr + 8 * k < a.M) && (C0 + 8 * L.lc < a.N));
-    const uint16_t* src = ok ? base + k * L.ld8 : a.x;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
-                 "l"(src), "r"(ok ? 16 : 0)
-                 : "memory");
-  }
-}
-
 template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
 __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) quant1d_kernel(const QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -215,40 +182,70 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
   }
   if (st_r || st_c) return;
 
-  const int64_t M = a.M, N = a.N;
+  const int64_t M = a.M, N = a.N, ld = a.ld;
   const int64_t nty = (M + kTM - 1) / kTM;
   const int64_t C0 = (int64_t)blockIdx.x * kTN;
+  const int cols = (int)((N - C0) < kTN ? (N - C0) : kTN);  // columns of this tile column (multiple of 16)
   const int tid = threadIdx.x;
   tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);  // read after the first barrier
   const CopyScales scR = make_scales(alpha_r, tbl);
   const CopyScales scC = make_scales(alpha_c, tbl + 128);
   const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
-  const Loader L = make_loader(tid, a.ld);
-  // fixed task coordinates of this thread
-  const int rb_b = tid & 15, rb_r0 = tid >> 4;   // rowwise: block column, first row
-  const int cp_p = tid & 127, cp_rb0 = tid >> 7; // columnwise: column pair, first row block
+
+  // Fixed per-thread roles and offsets (relative to a tile's origin):
+  //  loader     rows lr + 8k (k = 0..7), 16-byte chunk lc
+  //  rowwise    block column rb_b, rows rb_r0 + 16k (k = 0..3)
+  //  columnwise column pair cp_p, row blocks cp_rb0 + 2k (k = 0..1)
+  const int lr = tid >> 5, lc = tid & 31;
+  const bool lc_ok = 8 * lc < cols;
+  const int64_t ld_off = (int64_t)lr * ld + 8 * lc, ld_step = 8 * ld;
+  const uint32_t lds_off = lr * tile::kRowBytes + tile::swz(lc) * 16;
+  const int rb_b = tid & 15, rb_r0 = tid >> 4;
+  const bool rb_ok = 16 * rb_b < cols;
+  const int64_t hN = N / 2, sN = N / 16;
+  const int64_t q_off = (int64_t)rb_r0 * hN + 8 * rb_b, q_step = 16 * hN;
+  const int64_t s_off = (int64_t)rb_r0 * sN + rb_b, s_step = 16 * sN;
+  const int64_t c_off = (int64_t)rb_r0 * N + 16 * rb_b, c_step = 16 * N;  // SR counters, rowwise
+  const int cp_p = tid & 127, cp_rb0 = tid >> 7;
+  const bool cp_ok = 2 * cp_p < cols;
+
+  auto load = [&](uint8_t* buf, int64_t R0) {
+    const int64_t rl = M - R0;
+    const int rows = (int)(rl < kTM ? rl : kTM);
+    const uint16_t* src0 = a.x + R0 * ld + C0 + ld_off;
+    const uint32_t dst0 = tile::smem_u32(buf) + lds_off;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool ok = lc_ok && (lr + 8 * k < rows);
+      const uint16_t* src = ok ? src0 + k * ld_step : a.x;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+  };
 
   int64_t ty = blockIdx.y;
-  if (ty < nty) load_tile(bufs, a, L, ty * kTM, C0);
+  if (ty < nty) load(bufs, ty * kTM);
   tile::commit();
   for (int it = 0; ty < nty; ty += gridDim.y, ++it) {
     uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
     const int64_t tn = ty + gridDim.y;
-    if (tn < nty) load_tile(bufs + ((it + 1) & 1) * tile::kTileBytes, a, L, tn * kTM, C0);
+    if (tn < nty) load(bufs + ((it + 1) & 1) * tile::kTileBytes, tn * kTM);
     tile::commit();
     tile::wait_all_but_one();
     __syncthreads();
     const int64_t R0 = ty * kTM;
-    const tile::Coord tc = {R0, C0};
+    const int rows = (int)((M - R0) < kTM ? (M - R0) : kTM);
 
     // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
-    if (ROW) {
-      const int64_t gcol = C0 + 16 * rb_b;
+    if (ROW && rb_ok) {
+      uint8_t* qt = a.q_row + R0 * hN + C0 / 2 + q_off;
+      uint8_t* st = a.s_row + R0 * sN + C0 / 16 + s_off;
+      const uint64_t ct = a.ctr_off + (uint64_t)(R0 * N + C0 + c_off);
 #pragma unroll 1
       for (int k = 0; k < 4; ++k) {
         const int r = rb_r0 + 16 * k;
-        const int64_t grow = R0 + r;
-        if (grow >= M || gcol >= N) continue;
+        if (r >= rows) break;
         uint32_t wd[8];
         tile::read_row_block(buf, r, rb_b, wd);
         float z[16];
@@ -269,7 +266,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
         }
         uint32_t w[16];
         if (SR) {
-          const uint64_t base = a.ctr_off + (uint64_t)grow * (uint64_t)N + (uint64_t)gcol;
+          const uint64_t base = ct + (uint64_t)(k * c_step);
           uint32_t w1[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -289,21 +286,19 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
         uint2 codes;
         uint32_t e;
         quant_block16<Q46, SR, SEL>(z, bmax, scR, w, codes, e);
-        *reinterpret_cast<uint2*>(a.q_row + grow * (N / 2) + gcol / 2) = codes;
-        a.s_row[grow * (N / 16) + gcol / 16] = (uint8_t)e;
+        *reinterpret_cast<uint2*>(qt + k * q_step) = codes;
+        st[k * s_step] = (uint8_t)e;
       }
     }
     if (kStash) __syncthreads();
 
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
-    if (COL) {
+    if (COL && cp_ok) {
       const int p = cp_p;
-      const int64_t gcol = C0 + 2 * p;
 #pragma unroll 1
       for (int k = 0; k < 2; ++k) {
         const int rb = cp_rb0 + 2 * k;
-        const int64_t grow0 = R0 + 16 * rb;
-        if (gcol >= N || grow0 >= M) continue;
+        if (16 * rb >= rows) break;
         uint32_t wd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, p);
@@ -345,9 +340,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
                 w[i] = *reinterpret_cast<const uint32_t*>(stash + (16 * rb + i) * (kTN * 4) +
                                                           swz_stash(cc >> 2) * 16 + (cc & 3) * 4);
             } else {
+              const uint64_t base = a.ctr_off + (uint64_t)((R0 + 16 * rb) * N + C0 + cc);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                const uint2 ct = ctr_of(a.ctr_off + (uint64_t)(grow0 + i) * (uint64_t)N + (uint64_t)(gcol + h));
+                const uint2 ct = ctr_of(base + (uint64_t)i * (uint64_t)N);
                 w[i] = philox_w01(ct.x, ct.y, a.sr_k0, a.sr_k1).y;
               }
             }
@@ -362,7 +358,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
       }
     }
     __syncthreads();  // tile buffer free for the next prefetch; staging complete
-    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
+    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tile::Coord{R0, C0}, tid);
   }
 }
 
