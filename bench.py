@@ -271,6 +271,122 @@ def run_once(args):
     print(json.dumps({"once": args.workload, "flags": flags, "selection": sel}))
 
 
+def _time_kernels(nv, torch, xs, flags, sel, reps):
+    """Average durations (ms) of nvfp4_amax alone, nvfp4_quantize alone and the
+    step (both), each measured over `reps` CUDA-graph replays that rotate over
+    the input sets `xs` (no host launch gaps inside the timed region)."""
+    stream = torch.cuda.Stream()
+    am = [nv.nvfp4_amax(x, flags, synthetic.RHT_SEED) for x in xs]
+    outs = [nv.nvfp4_quantize(x, a, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED) for x, a in zip(xs, am)]
+    torch.cuda.synchronize()
+    graphs = {"amax": [], "quantize": [], "step": []}
+    for i, x in enumerate(xs):
+        for kind in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                if kind in ("amax", "step"):
+                    nv.nvfp4_amax(x, flags, synthetic.RHT_SEED, out=am[i])
+                if kind in ("quantize", "step"):
+                    nv.nvfp4_quantize(x, am[i], flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, out=outs[i])
+            graphs[kind].append(g)
+    torch.cuda.synchronize()
+    res = {}
+    with torch.cuda.stream(stream):
+        for kind, gl in graphs.items():
+            for r in range(len(gl)):
+                gl[r].replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(reps):
+                gl[r % len(gl)].replay()
+            e1.record(stream)
+            e1.synchronize()
+            res[kind] = e0.elapsed_time(e1) / reps
+    torch.cuda.synchronize()
+    for o in outs:
+        assert int(o.status.item()) == 0
+    return res["amax"], res["quantize"], res["step"]
+
+
+def _report_line(kind, name, M, N, flags, sel, amax_ms, quant_ms, step_ms, peak):
+    nb = algorithmic_bytes(M, N, flags)
+    q_gbs = nb / (quant_ms * 1e-3) / 1e9
+    step_gbs = nb / (step_ms * 1e-3) / 1e9
+    return {"report": kind, "name": name, "M": M, "N": N, "flags": flags, "selection": sel,
+            "amax_us": round(amax_ms * 1e3, 2), "quantize_us": round(quant_ms * 1e3, 2),
+            "step_us": round(step_ms * 1e3, 2),
+            "quantize_GBs": round(q_gbs, 1), "quantize_frac_of_measured_peak": round(q_gbs / peak, 4),
+            "step_GBs": round(step_gbs, 1), "step_frac_of_measured_peak": round(step_gbs / peak, 4),
+            "quantize_elements_per_s": round(M * N / (quant_ms * 1e-3), 1)}
+
+
+def run_report(args):
+    """One JSON line per measurement: every recipe workload, the 4/6, RHT and
+    SR ablations, and the size sweep of the activation (X) path from 2^20 to
+    2^30 elements.  Input/output sets rotate so that each step reads from HBM.
+    amax_us / quantize_us time each call alone (its input cold in L2);
+    step_us times amax then quantize, where quantize finds X in L2."""
+    import torch
+
+    import nvfp4_bit_block_gb300 as nv
+
+    nv.lib()
+    peak, _ = measured_peaks()
+    reps = max(5, args.steps)
+
+    def sets_of(bits_or_tensor, M, N, flags):
+        per_set = algorithmic_bytes(M, N, flags)
+        nsets = max(2, -(-3 * 128 * 2**20 // per_set))
+        if isinstance(bits_or_tensor, np.ndarray):
+            x0 = torch.from_numpy(bits_or_tensor.view(np.int16)).view(torch.bfloat16).cuda()
+        else:
+            x0 = bits_or_tensor
+        return [x0] + [x0.clone() for _ in range(nsets - 1)]
+
+    cache = {}
+    for name in synthetic.WORKLOADS:
+        flags, sel = synthetic.workload_flags(name)
+        bits = synthetic.workload(name)
+        M, N = bits.shape
+        xs = sets_of(bits, M, N, flags)
+        a, q, st = _time_kernels(nv, torch, xs, flags, sel, reps)
+        print(json.dumps(_report_line("workload", name, M, N, flags, sel, a, q, st, peak)), flush=True)
+        if name in ("act_46mae_8192x5120", "grad_rht_sr_16384x5120", "weight_2d_5120x20480"):
+            cache[name] = xs
+        else:
+            del xs
+    ablations = [("act_46mae_8192x5120", "RN rowwise+columnwise", 3, 0),
+                 ("act_46mae_8192x5120", "4/6 MAE", 67, 0), ("act_46mae_8192x5120", "4/6 MSE", 67, 1),
+                 ("act_46mae_8192x5120", "4/6 MAXERR", 67, 2), ("act_46mae_8192x5120", "RN rowwise only", 1, 0),
+                 ("act_46mae_8192x5120", "4/6 MAE rowwise only", 65, 0),
+                 ("grad_rht_sr_16384x5120", "RN", 3, 0), ("grad_rht_sr_16384x5120", "RHT(col)", 19, 0),
+                 ("grad_rht_sr_16384x5120", "SR", 35, 0), ("grad_rht_sr_16384x5120", "RHT(col)+SR", 51, 0),
+                 ("weight_2d_5120x20480", "1D RN", 3, 0), ("weight_2d_5120x20480", "2D RN", 7, 0),
+                 ("weight_2d_5120x20480", "2D 4/6 MAE", 71, 0)]
+    for wl, label, flags, sel in ablations:
+        xs = cache[wl]
+        M, N = xs[0].shape
+        a, q, st = _time_kernels(nv, torch, xs, flags, sel, reps)
+        print(json.dumps(_report_line("ablation", f"{wl}: {label}", M, N, flags, sel, a, q, st, peak)), flush=True)
+    cache.clear()
+    # size sweep of the X path (4/6-MSE, both copies), N = 4096, inputs drawn on the GPU
+    flags, sel = 67, 1
+    N = 4096
+    g = torch.Generator(device="cuda")
+    for k in range(20, 31):
+        M = (1 << k) // N
+        g.manual_seed(synthetic.DATA_SEED_BASE + 100 + k)
+        mult = torch.ones(N, device="cuda")
+        mult[torch.randperm(N, generator=g, device="cuda")[:2]] = 30.0
+        x0 = (torch.randn(M, N, generator=g, device="cuda") * mult).to(torch.bfloat16)
+        xs = sets_of(x0, M, N, flags)
+        a, q, st = _time_kernels(nv, torch, xs, flags, sel, reps)
+        print(json.dumps(_report_line("sweep", f"x_path_2^{k}", M, N, flags, sel, a, q, st, peak)), flush=True)
+        del xs, x0
+        torch.cuda.empty_cache()
+
+
 def run_oracle_sample(args, max_seconds: float = 20.0):
     """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
     import oracle
@@ -313,9 +429,14 @@ def main():
     ap.add_argument("--sel", type=int, default=None, help="override the workload's 4/6 selection rule")
     ap.add_argument("--once", action="store_true",
                     help="run amax + quantize three times on the workload and exit (for profilers)")
+    ap.add_argument("--report", action="store_true",
+                    help="print one JSON line per workload, ablation and X-path size (2^20..2^30)")
     args = ap.parse_args()
     if args.once:
         run_once(args)
+        return
+    if args.report:
+        run_report(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
   const float alpha_c = __fdiv_rn(A_c, den);
   const int st_r = ROW ? amax_status(A_r) : 0;
   const int st_c = COL ? amax_status(A_c) : 0;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.alpha[0] = alpha_r;
     a.alpha[1] = alpha_c;
     if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
@@ -183,9 +183,6 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
   if (st_r || st_c) return;
 
   const int64_t M = a.M, N = a.N, ld = a.ld;
-  const int64_t nty = (M + kTM - 1) / kTM;
-  const int64_t C0 = (int64_t)blockIdx.x * kTN;
-  const int cols = (int)((N - C0) < kTN ? (N - C0) : kTN);  // columns of this tile column (multiple of 16)
   const int tid = threadIdx.x;
   tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);  // read after the first barrier
   const CopyScales scR = make_scales(alpha_r, tbl);
@@ -197,26 +194,24 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
   //  rowwise    block column rb_b, rows rb_r0 + 16k (k = 0..3)
   //  columnwise column pair cp_p, row blocks cp_rb0 + 2k (k = 0..1)
   const int lr = tid >> 5, lc = tid & 31;
-  const bool lc_ok = 8 * lc < cols;
   const int64_t ld_off = (int64_t)lr * ld + 8 * lc, ld_step = 8 * ld;
   const uint32_t lds_off = lr * tile::kRowBytes + tile::swz(lc) * 16;
   const int rb_b = tid & 15, rb_r0 = tid >> 4;
-  const bool rb_ok = 16 * rb_b < cols;
   const int64_t hN = N / 2, sN = N / 16;
   const int64_t q_off = (int64_t)rb_r0 * hN + 8 * rb_b, q_step = 16 * hN;
   const int64_t s_off = (int64_t)rb_r0 * sN + rb_b, s_step = 16 * sN;
   const int64_t c_off = (int64_t)rb_r0 * N + 16 * rb_b, c_step = 16 * N;  // SR counters, rowwise
   const int cp_p = tid & 127, cp_rb0 = tid >> 7;
-  const bool cp_ok = 2 * cp_p < cols;
 
-  auto load = [&](uint8_t* buf, int64_t R0) {
-    const int64_t rl = M - R0;
-    const int rows = (int)(rl < kTM ? rl : kTM);
-    const uint16_t* src0 = a.x + R0 * ld + C0 + ld_off;
+  auto load = [&](uint8_t* buf, const tile::Coord& c) {
+    const int64_t rl = M - c.R0, cl = N - c.C0;
+    const int rows = (int)(rl < kTM ? rl : kTM), cols = (int)(cl < kTN ? cl : kTN);
+    const uint16_t* src0 = a.x + c.R0 * ld + c.C0 + ld_off;
     const uint32_t dst0 = tile::smem_u32(buf) + lds_off;
+    const bool col_ok = 8 * lc < cols;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const bool ok = lc_ok && (lr + 8 * k < rows);
+      const bool ok = col_ok && (lr + 8 * k < rows);
       const uint16_t* src = ok ? src0 + k * ld_step : a.x;
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
                    "l"(src), "r"(ok ? 16 : 0)
@@ -224,18 +219,23 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
     }
   };
 
-  int64_t ty = blockIdx.y;
-  if (ty < nty) load(bufs, ty * kTM);
+  tile::Walker w;
+  w.init(M, N);
+  if (w.valid()) load(bufs, w.coord());
   tile::commit();
-  for (int it = 0; ty < nty; ty += gridDim.y, ++it) {
+  for (int it = 0; w.valid(); w = w.next(), ++it) {
     uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
-    const int64_t tn = ty + gridDim.y;
-    if (tn < nty) load(bufs + ((it + 1) & 1) * tile::kTileBytes, tn * kTM);
+    const tile::Walker wn = w.next();
+    if (wn.valid()) load(bufs + ((it + 1) & 1) * tile::kTileBytes, wn.coord());
     tile::commit();
     tile::wait_all_but_one();
     __syncthreads();
-    const int64_t R0 = ty * kTM;
+    const tile::Coord tc = w.coord();
+    const int64_t R0 = tc.R0, C0 = tc.C0;
     const int rows = (int)((M - R0) < kTM ? (M - R0) : kTM);
+    const int cols = (int)((N - C0) < kTN ? (N - C0) : kTN);
+    const bool rb_ok = 16 * rb_b < cols;
+    const bool cp_ok = 2 * cp_p < cols;
 
     // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
     if (ROW && rb_ok) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
       }
     }
     __syncthreads();  // tile buffer free for the next prefetch; staging complete
-    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tile::Coord{R0, C0}, tid);
+    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
   }
 }
 
@@ -385,13 +385,11 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
     cap = (per_sm > 0 ? per_sm : 1) * sms;
     if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
   }
-  // columns of tiles across x; each CTA walks a strided set of row tiles
-  const int64_t ntx = (a.N + kTN - 1) / kTN, nty = (a.M + kTM - 1) / kTM;
-  int64_t gy = ntx > 0 ? cap / ntx : 1;
-  if (gy > nty) gy = nty;
-  if (gy < 1) gy = 1;
-  if (gy > 65535) gy = 65535;
-  const dim3 grid((unsigned)(ntx > 0 ? ntx : 1), (unsigned)gy, 1);
+  // persistent grid: every resident CTA slot, or one CTA per tile if fewer
+  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
+  int64_t g = ntiles < cap ? ntiles : cap;
+  if (g < 1) g = 1;
+  const dim3 grid((unsigned)g, 1, 1);
   kern<<<grid, kBlockThreads, kSmem, s>>>(a);
   return cudaGetLastError();
 }

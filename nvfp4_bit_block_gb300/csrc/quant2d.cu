@@ -89,8 +89,6 @@ __global__ void __launch_bounds__(kBlockThreads) quant2d_kernel(const QuantArgs 
   if (st) return;
 
   const int64_t M = a.M, N = a.N;
-  const int64_t ntx = (N + kTN - 1) / kTN;
-  const int64_t ntiles = ((M + kTM - 1) / kTM) * ntx;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ch = lane & 1, bcol = (lane >> 1) & 7, rh = lane >> 4;
   const int rb = warp >> 1;                                // row block of this warp
@@ -98,19 +96,19 @@ __global__ void __launch_bounds__(kBlockThreads) quant2d_kernel(const QuantArgs 
   const int chunk = tcol0 >> 3;
   const int trow0 = 16 * rb + 8 * rh;                      // first tile row of this thread
 
-  int64_t t = blockIdx.x;
-  if (t < ntiles) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, tile::coord(t, ntx), tid);
+  tile::Walker w;
+  w.init(M, N);
+  if (w.valid()) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, w.coord(), tid);
   tile::commit();
-  for (int it = 0; t < ntiles; t += gridDim.x, ++it) {
+  for (int it = 0; w.valid(); w = w.next(), ++it) {
     uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
-    const int64_t tn = t + gridDim.x;
-    if (tn < ntiles)
-      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld,
-                                      tile::coord(tn, ntx), tid);
+    const tile::Walker wn = w.next();
+    if (wn.valid())
+      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld, wn.coord(), tid);
     tile::commit();
     tile::wait_all_but_one();
     __syncthreads();
-    const tile::Coord tc = tile::coord(t, ntx);
+    const tile::Coord tc = w.coord();
     const int64_t grow0 = tc.R0 + trow0, gcol0 = tc.C0 + tcol0;
     // a block is valid when its 16 rows and 16 columns lie inside the tensor
     const bool valid = (tc.R0 + 16 * rb < M) && (tc.C0 + (tcol0 & ~15) < N);

@@ -40,10 +40,35 @@ struct Coord {
   int64_t R0, C0;
 };
 
-__device__ __forceinline__ Coord coord(int64_t t, int64_t ntx) {
-  const int64_t ty = t / ntx;
-  return {ty * kTM, (t - ty * ntx) * kTN};
-}
+// Tile walk of a persistent CTA: tiles t = blockIdx.x + k*gridDim.x in
+// row-major tile order (ntx tiles per row of tiles), with the (row, column)
+// tile coordinates advanced incrementally instead of divided per tile.
+struct Walker {
+  int64_t ty, tx;        // current tile
+  int64_t step_y, step_x; // gridDim.x = step_y * ntx + step_x
+  int64_t ntx, nty;
+  __device__ __forceinline__ void init(int64_t M, int64_t N) {
+    ntx = (N + kTN - 1) / kTN;
+    nty = (M + kTM - 1) / kTM;
+    if (ntx < 1) ntx = 1;
+    ty = blockIdx.x / ntx;
+    tx = blockIdx.x - ty * ntx;
+    step_y = gridDim.x / ntx;
+    step_x = gridDim.x - step_y * ntx;
+  }
+  __device__ __forceinline__ bool valid() const { return ty < nty; }
+  __device__ __forceinline__ Coord coord() const { return {ty * kTM, tx * kTN}; }
+  __device__ __forceinline__ Walker next() const {
+    Walker w = *this;
+    w.tx += step_x;
+    w.ty += step_y;
+    if (w.tx >= ntx) {
+      w.tx -= ntx;
+      w.ty += 1;
+    }
+    return w;
+  }
+};
 
 // Issue the async copies of one tile (NT threads, thread `tid`).
 template <int NT>
