@@ -12,19 +12,21 @@
 //     array; a persistent grid streams it with four 128-bit loads in flight per
 //     thread and a NaN-propagating packed bf16 abs-max;
 //   - amax_tile_kernel: a padded row stride or a transformed copy uses the
-//     quantize kernel's 64 x 256 shared-memory tile and its two passes.
+//     quantize kernels' persistent, double-buffered 64 x 256 shared-memory
+//     tiles (tile_pipeline.cuh) and their two passes.
 // Maxima are combined as the bit patterns of non-negative floats (unsigned
 // order equals float order, NaN above Inf); each CTA issues one atomicMax
 // per copy into the two output floats, which the host wrapper zeroes first.
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
+#include "tile_pipeline.cuh"
 
 namespace nvfp4 {
 namespace {
 
-constexpr int kTM = 64, kTN = 256, kRowBytes = kTN * 2, kBlockThreads = 256;
-
-__device__ __forceinline__ int swz_tile(int c) { return c ^ ((c >> 3) & 1); }
+using tile::kTM;
+using tile::kTN;
+constexpr int kBlockThreads = 256;
 
 __device__ __forceinline__ uint32_t absmax_nan_bf16x2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -85,46 +87,65 @@ __global__ void __launch_bounds__(kBlockThreads) amax_flat_kernel(const uint4* x
 
 template <bool RHT_ROW, bool RHT_COL>
 __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs a) {
-  __shared__ __align__(16) uint8_t tile[kTM * kRowBytes];
+  extern __shared__ __align__(16) uint8_t bufs[];  // 2 x 32 KB tiles
   const int64_t M = a.M, N = a.N;
-  const int64_t R0 = (int64_t)blockIdx.y * kTM, C0 = (int64_t)blockIdx.x * kTN;
   const int tid = threadIdx.x;
-  uint32_t m = 0u;
-  {
-    uint4 v[8];
+  const uint32_t signs = (RHT_ROW || RHT_COL) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
+  const int rb_b = tid & 15, rb_r0 = tid >> 4;    // rowwise tasks
+  const int cp_p = tid & 127, cp_rb0 = tid >> 7;  // columnwise tasks
+  uint32_t m_plain = 0u, m_row = 0u, m_col = 0u;
+
+  tile::Walker w;
+  w.init(M, N);
+  if (w.valid()) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, w.coord(), tid);
+  tile::commit();
+  for (int it = 0; w.valid(); w = w.next(), ++it) {
+    const uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
+    const tile::Walker wn = w.next();
+    if (wn.valid())
+      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld, wn.coord(), tid);
+    tile::commit();
+    tile::wait_all_but_one();
+    __syncthreads();
+    const tile::Coord tc = w.coord();
+    const int rows = (int)((M - tc.R0) < kTM ? (M - tc.R0) : kTM);
+    const int cols = (int)((N - tc.C0) < kTN ? (N - tc.C0) : kTN);
+    if (RHT_COL || !RHT_ROW) {
+      // columnwise tasks: plain max of every element, and the transformed
+      // column vectors' max when the columnwise copy has the RHT
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        const int rb = cp_rb0 + 2 * k;
+        if (2 * cp_p >= cols || 16 * rb >= rows) continue;
+        uint32_t wd[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int id = tid + k * kBlockThreads;
-      const int r = id >> 5, c = id & 31;
-      const int64_t grow = R0 + r, gcol = C0 + 8 * c;
-      v[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (grow < M && gcol < N) v[k] = ld_stream(a.x + grow * a.ld + gcol);
-    }
+        for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, cp_p);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      m = absmax_nan_bf16x2(m, absmax_nan_bf16x2(absmax_nan_bf16x2(v[k].x, v[k].y),
-                                                 absmax_nan_bf16x2(v[k].z, v[k].w)));
-      if (RHT_ROW || RHT_COL) {
-        const int id = tid + k * kBlockThreads;
-        const int r = id >> 5, c = id & 31;
-        *reinterpret_cast<uint4*>(tile + r * kRowBytes + swz_tile(c) * 16) = v[k];
+        for (int i = 0; i < 16; i += 2) m_plain = absmax_nan_bf16x2(m_plain, absmax_nan_bf16x2(wd[i], wd[i + 1]));
+        if (RHT_COL) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = h ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
+            rht16(z, signs);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m_col = max(m_col, abs_bits(z[i]));
+          }
+        }
       }
     }
-  }
-  const uint32_t plain = packed_to_bits(m);
-  uint32_t m_row = 0u, m_col = 0u;
-  if (RHT_ROW || RHT_COL) {
-    __syncthreads();
-    const uint32_t signs = rht_sign_bits(a.rht_k0, a.rht_k1);
     if (RHT_ROW) {
 #pragma unroll 1
-      for (int k = 0; k < kTM * 16 / kBlockThreads; ++k) {
-        const int task = tid + k * kBlockThreads;
-        const int r = task >> 4, b = task & 15;
-        if (R0 + r >= M || C0 + 16 * b >= N) continue;
-        const uint4 lo = *reinterpret_cast<const uint4*>(tile + r * kRowBytes + swz_tile(2 * b) * 16);
-        const uint4 hi = *reinterpret_cast<const uint4*>(tile + r * kRowBytes + swz_tile(2 * b + 1) * 16);
-        const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      for (int k = 0; k < 4; ++k) {
+        const int r = rb_r0 + 16 * k;
+        if (16 * rb_b >= cols || r >= rows) continue;
+        uint32_t wd[8];
+        tile::read_row_block(buf, r, rb_b, wd);
+        if (!RHT_COL) {
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) m_plain = absmax_nan_bf16x2(m_plain, absmax_nan_bf16x2(wd[i], wd[i + 1]));
+        }
         float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -136,30 +157,36 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
         for (int j = 0; j < 16; ++j) m_row = max(m_row, abs_bits(z[j]));
       }
     }
-    if (RHT_COL) {
-#pragma unroll 1
-      for (int k = 0; k < (kTN / 2) * (kTM / 16) / kBlockThreads; ++k) {
-        const int task = tid + k * kBlockThreads;
-        const int p = task & 127, rb = task >> 7;
-        if (C0 + 2 * p >= N || R0 + 16 * rb >= M) continue;
-        uint32_t wd[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          wd[i] = *reinterpret_cast<const uint32_t*>(tile + (16 * rb + i) * kRowBytes + swz_tile(p >> 2) * 16 +
-                                                     (p & 3) * 4);
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float z[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) z[i] = h ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
-          rht16(z, signs);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) m_col = max(m_col, abs_bits(z[i]));
-        }
-      }
-    }
+    __syncthreads();  // the buffer is refilled by the next iteration's prefetch
   }
+  const uint32_t plain = packed_to_bits(m_plain);
   cta_reduce_and_publish(RHT_ROW ? m_row : plain, RHT_COL ? m_col : plain, a.amax);
+}
+
+template <bool RHT_ROW, bool RHT_COL>
+cudaError_t launch_tile(const AmaxArgs& a, cudaStream_t s) {
+  constexpr int kSmem = 2 * tile::kTileBytes;
+  auto kern = amax_tile_kernel<RHT_ROW, RHT_COL>;
+  static int grid_cap[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int cap = (dev >= 0 && dev < 64) ? grid_cap[dev] : 0;
+  if (cap == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockThreads, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cap = (per_sm > 0 ? per_sm : 1) * sms;
+    if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
+  }
+  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
+  int64_t g = ntiles < cap ? ntiles : cap;
+  if (g < 1) g = 1;
+  kern<<<(unsigned)g, kBlockThreads, kSmem, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -177,17 +204,10 @@ cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStrea
                                                               a.amax);
     return cudaGetLastError();
   }
-  const int64_t gx = (a.N + kTN - 1) / kTN, gy = (a.M + kTM - 1) / kTM;
-  const dim3 grid((unsigned)gx, (unsigned)gy, 1);
-  if (rht_row && rht_col)
-    amax_tile_kernel<true, true><<<grid, kBlockThreads, 0, s>>>(a);
-  else if (rht_row)
-    amax_tile_kernel<true, false><<<grid, kBlockThreads, 0, s>>>(a);
-  else if (rht_col)
-    amax_tile_kernel<false, true><<<grid, kBlockThreads, 0, s>>>(a);
-  else
-    amax_tile_kernel<false, false><<<grid, kBlockThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (rht_row && rht_col) return launch_tile<true, true>(a, s);
+  if (rht_row) return launch_tile<true, false>(a, s);
+  if (rht_col) return launch_tile<false, true>(a, s);
+  return launch_tile<false, false>(a, s);
 }
 
 }  // namespace nvfp4
