@@ -39,6 +39,17 @@ METRIC = "NVFP4 quantize GB/s (bf16 in + fp4/scales out), % of GB300 HBM peak"
 UNIT = "GB/s"
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def algorithmic_bytes(M: int, N: int, flags: int) -> int:
     """bf16 read + per copy (codes N*M/2 + scales N*M/16)."""
     copies = (1 if flags & 1 else 0) + (1 if flags & 2 else 0)
@@ -169,11 +180,7 @@ def run_ours(args, rank: int, world: int):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
 
     # per-kernel durations inside the same rotating stream of steps, launched
     # directly with an event between the two kernels, for the roofline of the
@@ -195,24 +202,50 @@ def run_ours(args, rank: int, world: int):
         status = int(o.status.item())
         assert status == 0, f"quantize reported status {status}"
 
-    # end to end through the public API: pinned host x -> device -> amax ->
-    # quantize -> outputs back to pinned host buffers, every step
-    host_out = [torch.empty(t_.shape, dtype=t_.dtype, pin_memory=True)
-                for t_ in (out.q_row, out.s_row, out.q_col, out.s_col, out.alpha) if t_ is not None]
-    dev_out = [t_ for t_ in (out.q_row, out.s_row, out.q_col, out.s_col, out.alpha) if t_ is not None]
-    e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        for k in range(2 + e2e_steps):
-            if k == 2:
-                torch.cuda.synchronize()
-                t0 = time.perf_counter()
-            x.copy_(x_host, non_blocking=True)
-            step(0)
-            for h, d in zip(host_out, dev_out):
+    # End to end through the public API: every step copies its input from
+    # pinned host memory to the device, runs amax + quantize and copies all
+    # outputs back to pinned host memory.  Steps are pipelined the way a
+    # stream of tensors would be: copy-in, compute and copy-out run on their
+    # own streams, ordered by events, over two device buffer sets (the input
+    # and output of set i are reused two steps later).
+    e2e_steps = max(4, min(args.steps, 12))
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dev_outs = [[t_ for t_ in (o.q_row, o.s_row, o.q_col, o.s_col, o.alpha) if t_ is not None] for o in outs[:2]]
+    host_outs = [[torch.empty(t_.shape, dtype=t_.dtype, pin_memory=True) for t_ in d] for d in dev_outs]
+    x_hosts = [x_host, x_host.clone().pin_memory()]
+    ev_in = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
+    ev_comp = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
+    ev_out = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
+    torch.cuda.synchronize()
+
+    def e2e_step(k):
+        i = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_comp[k - 2])     # set i's input no longer read
+            xs[i].copy_(x_hosts[i], non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[k])
+            if k >= 2:
+                stream.wait_event(ev_out[k - 2])    # set i's outputs copied out
+            step(i)
+            ev_comp[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            for h, d in zip(host_outs[i], dev_outs[i]):
                 h.copy_(d, non_blocking=True)
-        stream.synchronize()
+            ev_out[k].record(s_out)
+
+    for k in range(2):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(2, 2 + e2e_steps):
+        e2e_step(k)
+    torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    d2h = sum(t_.numel() * t_.element_size() for t_ in dev_out)
+    d2h = sum(t_.numel() * t_.element_size() for t_ in dev_outs[0])
 
     nbytes = algorithmic_bytes(M, N, flags)
     value = nbytes * args.steps / (total_ms * 1e-3) / 1e9 * world
