@@ -69,8 +69,11 @@ typedef enum {
                                an RHT flag for a copy not requested; bad selector    */
   NVFP4_ERR_CUDA = -5,      /* a CUDA launch or copy failed                           */
   NVFP4_ERR_NONFINITE = -6, /* device status: amax is Inf or NaN                      */
-  NVFP4_ERR_RANGE = -7      /* device status: 0 < amax < 2^-100 (the per-block
+  NVFP4_ERR_RANGE = -7,     /* device status: 0 < amax < 2^-100 (the per-block
                                reciprocal could overflow FP32)                        */
+  NVFP4_ERR_PIPELINE = -8   /* device status: a tile copy into shared memory did not
+                               complete within about a second; the kernel stopped
+                               and the outputs are incomplete                         */
 } nvfp4_status;
 
 enum {
@@ -136,7 +139,8 @@ NVFP4_API int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, ui
  *   alpha_dev       float[2] (device): alpha of R and C, always written
  *   status_dev      int (device) or NULL: set to NVFP4_ERR_NONFINITE or
  *                   NVFP4_ERR_RANGE when a requested copy's amax is not usable,
- *                   in which case no code or scale byte is written; left
+ *                   in which case no code or scale byte is written, or to
+ *                   NVFP4_ERR_PIPELINE when a tile load timed out; left
  *                   untouched on success (the caller zeroes it)
  * With 2D, the tile scale is repeated in the 1x16 scale layouts (16 times in
  * s_row, 16 times in s_col) and C's codes are exactly the transpose of R's.

@@ -37,6 +37,9 @@ int check_shape(int64_t M, int64_t N, int64_t ld, uint32_t flags) {
 // Test hook: when set, the next launch reports a CUDA failure without
 // enqueueing anything (exercises the NVFP4_ERR_CUDA path on any machine).
 int g_fail_next_launch = 0;
+// Test hook: the next 1D quantize arms its tile barriers but issues no copy,
+// so its bounded waits run out and it reports NVFP4_ERR_PIPELINE.
+int g_skip_next_copy = 0;
 
 int launch_status(cudaError_t e) {
   if (g_fail_next_launch) {
@@ -117,6 +120,8 @@ int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const fl
   a.sel = (flags & NVFP4_46) ? sel : NVFP4_SEL_MAE;
   a.rht_row = (flags & NVFP4_RHT_ROW) ? 1 : 0;
   a.rht_col = (flags & NVFP4_RHT_COL) ? 1 : 0;
+  a.test_skip_copy = g_skip_next_copy;
+  g_skip_next_copy = 0;
   const bool q46 = (flags & NVFP4_46) != 0, sr = (flags & NVFP4_SR) != 0;
   if (g_fail_next_launch) return launch_status(cudaSuccess);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -152,6 +157,7 @@ const char* nvfp4_strerror(int status) {
     case NVFP4_ERR_CUDA: return "CUDA launch failed";
     case NVFP4_ERR_NONFINITE: return "amax is Inf or NaN";
     case NVFP4_ERR_RANGE: return "amax below 2^-100";
+    case NVFP4_ERR_PIPELINE: return "a tile copy did not arrive within the wait limit";
     default: return "unknown status";
   }
 }
@@ -159,5 +165,10 @@ const char* nvfp4_strerror(int status) {
 // Test hook (not declared in nvfp4.h): make the next launch report
 // NVFP4_ERR_CUDA without enqueueing anything.
 NVFP4_API void nvfp4_test_fail_next_launch(void) { g_fail_next_launch = 1; }
+
+// Test hook (not declared in nvfp4.h): the next 1D nvfp4_quantize issues no
+// tile copy, so it stops after its bounded wait with NVFP4_ERR_PIPELINE in
+// status_dev.
+NVFP4_API void nvfp4_test_skip_next_copy(void) { g_skip_next_copy = 1; }
 
 }  // extern "C"

@@ -26,6 +26,7 @@ constexpr float kMinAmax = 0x1p-100f;   // below this the per-block reciprocal m
 // status values written to the device status word (same integers as nvfp4.h)
 constexpr int kStatusNonFinite = -6;
 constexpr int kStatusRange = -7;
+constexpr int kStatusPipeline = -8;
 
 // ---------------------------------------------------------------- bf16
 // Exact widening of the low / high bf16 half of a word by bit placement
@@ -228,13 +229,20 @@ __device__ __forceinline__ BlockScale block_scale(float b, float alpha, float Q)
 // b * (1/den), which is within 2 ulp of fl(b / den); the two give the same
 // E4M3 byte unless an E4M3 rounding midpoint (fp32 bits 19..0 == 0x80000 in
 // the normal range) lies within 3 ulp, or the value is in E4M3's subnormal
-// range -- then the IEEE division decides.  rden = 1/den, correctly rounded.
-__device__ __forceinline__ uint32_t scale_byte(float b, float den, float rden) {
-  if (!(b > 0.0f)) return 0u;
-  float t = __fmul_rn(b, rden);
-  const uint32_t low = __float_as_uint(t) & 0xFFFFFu;
-  if (low - 0x7FFFDu < 7u || t < 0x1p-6f) t = __fdiv_rn(b, den);
-  return e4m3_encode(t);
+// range.  Such blocks (a few in a million) are flagged in `exact_needed` and
+// redone by the caller with the IEEE division (scale_byte_exact); keeping
+// that division out of the main path leaves it free of branches.
+// rden = 1/den, correctly rounded.
+__device__ __forceinline__ uint32_t scale_byte_fast(float b, float rden, bool& exact_needed) {
+  const float t = __fmul_rn(b, rden);
+  const uint32_t u = __float_as_uint(t);
+  // bits 19..0 of t within [0x7FFFD, 0x80004], or 0 < t < 2^-6 (t >= 0 here)
+  exact_needed = exact_needed || ((u + 3u) & 0xFFFF8u) == 0x80000u || u - 1u < 0x3C7FFFFFu;
+  return e4m3_encode(t);  // b == 0 gives t == 0 and byte 0
+}
+
+__device__ __forceinline__ uint32_t scale_byte_exact(float b, float den) {
+  return (b > 0.0f) ? e4m3_encode(__fdiv_rn(b, den)) : 0u;
 }
 
 // Per-copy table of d = e*alpha and 1/d for every scale byte e (0..127),

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
@@ -22,6 +23,7 @@ struct QuantArgs {
   uint32_t rht_k0, rht_k1;
   int sel;
   int rht_row, rht_col;
+  int test_skip_copy;  // test hook: arm the first tile's barrier but issue no copy
 };
 
 struct AmaxArgs {
@@ -39,6 +41,11 @@ struct DequantArgs {
   int out_bf16;
   void* out;
 };
+
+// TMA boxes of the bf16 input: 64 columns (128 bytes, the swizzle span) x 64 rows.
+constexpr int kBoxCols = 64;
+constexpr int kBoxRows = 64;
+cudaError_t make_tile_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t N, int64_t ld);
 
 cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);

@@ -2,9 +2,11 @@
 // quant1d_kernel.cuh -- fused rowwise + columnwise NVFP4 quantization with 1x16 blocks.
 //
 // One read of X produces both copies.  Persistent CTAs stream 64 x 256 bf16
-// tiles through double-buffered shared memory (tile_pipeline.cuh), then
+// tiles into double-buffered shared memory with TMA bulk tensor copies (four
+// 64 x 64 boxes per tile, 128-byte swizzle, completion on an mbarrier; one
+// thread issues them while the CTA works on the other buffer), then
 //   - the rowwise pass gives each thread whole 16-column blocks (two 128-bit
-//     shared loads) and stores their codes directly (coalesced), and
+//     shared loads) and stores their codes directly (32 bytes per row), and
 //   - the columnwise pass gives each thread a column pair over 16 rows (sixteen
 //     32-bit shared loads, one bf16x2 word per row) and stages the codes, so
 //     that each column of the transposed copy is written as one 32-byte store,
@@ -22,6 +24,9 @@
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 #include "tile_pipeline.cuh"
+#include "tma.cuh"
+
+#include <type_traits>
 
 #ifndef NVFP4_Q1D_MIN_CTAS
 #define NVFP4_Q1D_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for
@@ -35,8 +40,15 @@ using tile::kTN;
 constexpr int kStashBytes = kTM * kTN * 4;  // Philox word 1 per element, 64 KB
 constexpr int kBlockThreads = 256;
 
-// 16-byte chunk q of a stash row (64 chunks) lives at chunk q ^ ((q >> 3) & 7)
-__device__ __forceinline__ int swz_stash(int q) { return q ^ ((q >> 3) & 7); }
+// Byte offset of the stash word of tile row r, tile column c.  A row is
+// 1 KB (256 words); its 16-byte chunk q = c / 4 sits at
+// q ^ ((q >> 3) & 7) ^ ((r & 1) << 1), so that the rowwise pass's 16-byte
+// stores from a quarter warp (two rows, four blocks) fall in eight distinct
+// bank groups.
+__device__ __forceinline__ uint32_t stash_off(int r, int c) {
+  const int q = c >> 2;
+  return (uint32_t)r * 1024u + (uint32_t)((q ^ ((q >> 3) & 7) ^ ((r & 1) << 1)) << 4) + (uint32_t)(c & 3) * 4u;
+}
 
 __device__ __forceinline__ uint2 ctr_of(uint64_t i) { return make_uint2((uint32_t)i, (uint32_t)(i >> 32)); }
 
@@ -137,10 +149,12 @@ __device__ __forceinline__ float candidate16(const float* z, uint32_t e, float2 
 
 // One block: the standard max-6 candidate and, with 4/6, the max-4 candidate;
 // the max-4 one is kept only if its score is strictly lower.
-template <bool Q46, bool SR, int SEL>
+// EXACT = false: scale bytes from the fast product, `redo` set when the
+// block needs the IEEE division; EXACT = true: the division itself.
+template <bool Q46, bool SR, int SEL, bool EXACT>
 __device__ __forceinline__ void quant_block16(const float* z, float bmax, const CopyScales& sc, const uint32_t* w,
-                                              uint2& codes, uint32_t& e) {
-  const uint32_t e6 = scale_byte(bmax, sc.den6, sc.rden6);
+                                              uint2& codes, uint32_t& e, bool& redo) {
+  const uint32_t e6 = EXACT ? scale_byte_exact(bmax, sc.den6) : scale_byte_fast(bmax, sc.rden6, redo);
   const float2 di6 = sc.tbl[e6];
   if (!Q46) {
     float v[16];
@@ -151,22 +165,32 @@ __device__ __forceinline__ void quant_block16(const float* z, float bmax, const 
   }
   uint2 c6, c4;
   const float s6 = candidate16<SR, SEL>(z, e6, di6, 6.0f, w, c6);
-  const uint32_t e4 = scale_byte(bmax, sc.den4, sc.rden4);
+  const uint32_t e4 = EXACT ? scale_byte_exact(bmax, sc.den4) : scale_byte_fast(bmax, sc.rden4, redo);
   const float s4 = candidate16<SR, SEL>(z, e4, sc.tbl[e4], 4.0f, w, c4);
   const bool four = s4 < s6;
   codes = four ? c4 : c6;
   e = four ? e4 : e6;
 }
 
-template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
-__global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) quant1d_kernel(const QuantArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+// RHT bit 0: Hadamard on the rowwise copy; bit 1: on the columnwise copy.
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL, int RHT>
+__global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
+    quant1d_kernel(const QuantArgs a, const __grid_constant__ CUtensorMap xmap) {
+  constexpr bool kRhtRow = (RHT & 1) != 0, kRhtCol = (RHT & 2) != 0;
+  extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kStash = SR && ROW && COL;
-  uint8_t* bufs = smem;                                      // 2 x 32 KB tiles
-  uint8_t* cstage = smem + 2 * tile::kTileBytes;             // 8 KB
+  // With the 64 KB stash a second tile buffer would leave room for one CTA
+  // per SM; a single buffer fits two, whose loads overlap each other's math.
+  constexpr bool kDB = !kStash;
+  constexpr int kBufs = kDB ? 2 : 1;
+  uint8_t* bufs = smem;                                      // 1 or 2 x 32 KB tiles (1024-aligned)
+  uint8_t* cstage = smem + kBufs * tile::kTileBytes;         // 8 KB
   uint8_t* sstage = cstage + tile::kCStageBytes;             // 1 KB
   float2* tbl = reinterpret_cast<float2*>(sstage + tile::kSStageBytes);  // 2 x 128 (d, 1/d)
   uint8_t* stash = reinterpret_cast<uint8_t*>(tbl + 256);    // 64 KB with kStash
+  // Scale bytes never exceed 0x7E (448), so entry 127 of each table is free:
+  // it holds the tile barrier of buffer 0 (R table) and buffer 1 (C table).
+  const uint32_t bar0 = tile::smem_u32(tbl + 127), bar1 = tile::smem_u32(tbl + 255);
 
   // a2: alpha = amax / (6*448), or amax / (6*256) with 4/6
   const float den = Q46 ? kAlphaDen46 : kAlphaDen;
@@ -175,79 +199,100 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
   const float alpha_c = __fdiv_rn(A_c, den);
   const int st_r = ROW ? amax_status(A_r) : 0;
   const int st_c = COL ? amax_status(A_c) : 0;
+  const bool misaligned = (tile::smem_u32(smem) & 1023u) != 0u;  // the 128-byte swizzle needs 1 KB alignment
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.alpha[0] = alpha_r;
     a.alpha[1] = alpha_c;
     if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
+    if (misaligned && !(st_r || st_c) && a.status) *a.status = kStatusPipeline;
   }
-  if (st_r || st_c) return;
+  if (st_r || st_c || misaligned) return;
 
-  const int64_t M = a.M, N = a.N, ld = a.ld;
+  const int64_t M = a.M, N = a.N;
   const int tid = threadIdx.x;
-  tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);  // read after the first barrier
+  if ((tid & 127) != 127) tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);
+  if (tid == 0) {
+    tma::mbar_init(bar0, 1);
+    tma::mbar_init(bar1, 1);
+    tma::fence_barrier_init();
+  }
+  __syncthreads();  // barriers and tables ready
   const CopyScales scR = make_scales(alpha_r, tbl);
   const CopyScales scC = make_scales(alpha_c, tbl + 128);
-  const uint32_t signs = (a.rht_row || a.rht_col) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
+  const uint32_t signs = (kRhtRow || kRhtCol) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
 
-  // Fixed per-thread roles and offsets (relative to a tile's origin):
-  //  loader     rows lr + 8k (k = 0..7), 16-byte chunk lc
-  //  rowwise    block column rb_b, rows rb_r0 + 16k (k = 0..3)
-  //  columnwise column pair cp_p, row blocks cp_rb0 + 2k (k = 0..1)
-  const int lr = tid >> 5, lc = tid & 31;
-  const int64_t ld_off = (int64_t)lr * ld + 8 * lc, ld_step = 8 * ld;
-  const uint32_t lds_off = lr * tile::kRowBytes + tile::swz(lc) * 16;
-  const int rb_b = tid & 15, rb_r0 = tid >> 4;
+  // Shared tile = four 64-column boxes as the TMA writes them: box j at
+  // 8 KB * j, row r at 128 * r, 16-byte chunk c at (c ^ (r & 7)) * 16.
+  // Fixed per-thread roles (relative to a tile's origin):
+  //  rowwise    tile row rr = 8*warp + lane/4, blocks rq + 4k (k = 0..3):
+  //             block rq + 4k is chunks 2rq, 2rq+1 of box k, so a quarter
+  //             warp (rows rr, rr+1; four blocks each) hits eight distinct
+  //             bank groups, and each row's four code words are 32 bytes
+  //  columnwise column pair cp_p, row blocks cp_rb0 + 2k (k = 0..1): a warp
+  //             reads one 128-byte box row per load
+  const int lane = tid & 31;
+  const int rr = 8 * (tid >> 5) + (lane >> 2), rq = lane & 3;
+  const uint32_t r_chunk0 = rr * 128 + ((uint32_t)((2 * rq) ^ (lane >> 2)) << 4);  // second chunk: ^ 16
   const int64_t hN = N / 2, sN = N / 16;
-  const int64_t q_off = (int64_t)rb_r0 * hN + 8 * rb_b, q_step = 16 * hN;
-  const int64_t s_off = (int64_t)rb_r0 * sN + rb_b, s_step = 16 * sN;
-  const int64_t c_off = (int64_t)rb_r0 * N + 16 * rb_b, c_step = 16 * N;  // SR counters, rowwise
   const int cp_p = tid & 127, cp_rb0 = tid >> 7;
+  const uint32_t c_base = (cp_p >> 5) * 8192 + (cp_p & 3) * 4;
+  const uint32_t c_chunk = (uint32_t)((cp_p & 31) >> 2) << 4;
 
-  auto load = [&](uint8_t* buf, const tile::Coord& c) {
-    const int64_t rl = M - c.R0, cl = N - c.C0;
-    const int rows = (int)(rl < kTM ? rl : kTM), cols = (int)(cl < kTN ? cl : kTN);
-    const uint16_t* src0 = a.x + c.R0 * ld + c.C0 + ld_off;
-    const uint32_t dst0 = tile::smem_u32(buf) + lds_off;
-    const bool col_ok = 8 * lc < cols;
+  auto issue = [&](int b, const tile::Coord& c) {
+    const uint32_t bar = b ? bar1 : bar0;
+    tma::arrive_expect_tx(bar, tile::kTileBytes);
+    if (a.test_skip_copy) return;
+    const uint32_t dst = tile::smem_u32(bufs + b * tile::kTileBytes);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const bool ok = col_ok && (lr + 8 * k < rows);
-      const uint16_t* src = ok ? src0 + k * ld_step : a.x;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + k * 8 * tile::kRowBytes),
-                   "l"(src), "r"(ok ? 16 : 0)
-                   : "memory");
-    }
+    for (int j = 0; j < 4; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
   };
 
   tile::Walker w;
   w.init(M, N);
-  if (w.valid()) load(bufs, w.coord());
-  tile::commit();
+  if (tid == 0 && w.valid()) issue(0, w.coord());
   for (int it = 0; w.valid(); w = w.next(), ++it) {
-    uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
-    const tile::Walker wn = w.next();
-    if (wn.valid()) load(bufs + ((it + 1) & 1) * tile::kTileBytes, wn.coord());
-    tile::commit();
-    tile::wait_all_but_one();
-    __syncthreads();
+    const int b = kDB ? (it & 1) : 0;
+    uint8_t* buf = bufs + b * tile::kTileBytes;
+    if (tid == 0) {
+      if (kDB) {
+        const tile::Walker wn = w.next();
+        if (wn.valid()) issue(b ^ 1, wn.coord());  // that buffer was released by the last barrier
+      } else if (it > 0) {
+        issue(0, w.coord());
+      }
+    }
+    const uint32_t parity = kDB ? ((it >> 1) & 1) : (it & 1);
+    const bool arrived = tma::wait(b ? bar1 : bar0, parity);
+    if (!__syncthreads_and(arrived)) {
+      // a copy did not arrive in time: report it, give the copies in flight
+      // one more bounded wait, and stop
+      if (tid == 0) {
+        if (a.status) atomicExch(a.status, kStatusPipeline);
+        tma::wait(b ? bar1 : bar0, parity);
+        if (kDB && w.next().valid()) tma::wait(b ? bar0 : bar1, ((it + 1) >> 1) & 1);
+      }
+      return;
+    }
     const tile::Coord tc = w.coord();
     const int64_t R0 = tc.R0, C0 = tc.C0;
     const int rows = (int)((M - R0) < kTM ? (M - R0) : kTM);
     const int cols = (int)((N - C0) < kTN ? (N - C0) : kTN);
-    const bool rb_ok = 16 * rb_b < cols;
     const bool cp_ok = 2 * cp_p < cols;
 
     // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
-    if (ROW && rb_ok) {
-      uint8_t* qt = a.q_row + R0 * hN + C0 / 2 + q_off;
-      uint8_t* st = a.s_row + R0 * sN + C0 / 16 + s_off;
-      const uint64_t ct = a.ctr_off + (uint64_t)(R0 * N + C0 + c_off);
-#pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
-        const int r = rb_r0 + 16 * k;
-        if (r >= rows) break;
+    if (ROW && rr < rows) {
+      uint8_t* qt = a.q_row + (R0 + rr) * hN + C0 / 2 + 8 * rq;
+      uint8_t* st = a.s_row + (R0 + rr) * sN + C0 / 16 + rq;
+      const uint64_t ct = a.ctr_off + (uint64_t)((R0 + rr) * N + C0 + 16 * rq);
+      // block rq + 4k of row rr; returns whether the block needs the exact scale path
+      auto rblock = [&](int k, auto exact) -> bool {
         uint32_t wd[8];
-        tile::read_row_block(buf, r, rb_b, wd);
+        {
+          const uint4 lo = *reinterpret_cast<const uint4*>(buf + k * 8192 + r_chunk0);
+          const uint4 hi = *reinterpret_cast<const uint4*>(buf + k * 8192 + (r_chunk0 ^ 16u));
+          wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
+          wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
+        }
         float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -256,7 +301,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
           z[2 * j + 1] = f.y;
         }
         float bmax;
-        if (a.rht_row) {
+        if (kRhtRow) {
           rht16(z, signs);
           bmax = 0.0f;
 #pragma unroll
@@ -266,7 +311,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
         }
         uint32_t w[16];
         if (SR) {
-          const uint64_t base = ct + (uint64_t)(k * c_step);
+          const uint64_t base = ct + (uint64_t)(64 * k);
           uint32_t w1[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -276,18 +321,30 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
             w1[j] = pw.y;
           }
           if (kStash) {
-            uint8_t* srow = stash + r * (kTN * 4);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(srow + swz_stash(4 * rb_b + q) * 16) =
+              *reinterpret_cast<uint4*>(stash + stash_off(rr, 16 * (rq + 4 * k) + 4 * q)) =
                   make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
           }
         }
         uint2 codes;
         uint32_t e;
-        quant_block16<Q46, SR, SEL>(z, bmax, scR, w, codes, e);
-        *reinterpret_cast<uint2*>(qt + k * q_step) = codes;
-        st[k * s_step] = (uint8_t)e;
+        bool redo = false;
+        quant_block16<Q46, SR, SEL, decltype(exact)::value>(z, bmax, scR, w, codes, e, redo);
+        *reinterpret_cast<uint2*>(qt + 32 * k) = codes;
+        st[4 * k] = (uint8_t)e;
+        return redo;
+      };
+      uint32_t redo = 0u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (16 * (rq + 4 * k) >= cols) break;
+        if (rblock(k, std::false_type{})) redo |= 1u << k;
+      }
+      if (redo) {  // rare: redo those blocks with the exact scale bytes
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k)
+          if (redo & (1u << k)) rblock(k, std::true_type{});
       }
     }
     if (kStash) __syncthreads();
@@ -295,16 +352,16 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
     if (COL && cp_ok) {
       const int p = cp_p;
-#pragma unroll 1
-      for (int k = 0; k < 2; ++k) {
-        const int rb = cp_rb0 + 2 * k;
-        if (16 * rb >= rows) break;
+      // row block rb of column pair p; returns whether a block needs the exact scale path
+      auto ctask = [&](int rb, auto exact) -> bool {
         uint32_t wd[16];
+        const uint8_t* cb = buf + c_base + rb * 2048;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, p);
+        for (int i = 0; i < 16; ++i)
+          wd[i] = *reinterpret_cast<const uint32_t*>(cb + i * 128 + (c_chunk ^ ((uint32_t)(i & 7) << 4)));
         // both columns' maxima at once (low half = column 2p, high half = 2p+1)
         uint32_t m2 = 0u;
-        if (!a.rht_col) {
+        if (!kRhtCol) {
           uint32_t t8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) t8[i] = absmax_bf16x2(wd[2 * i], wd[2 * i + 1]);
@@ -321,11 +378,12 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
           zz[0][i] = f.x;
           zz[1][i] = f.y;
         }
+        bool redo = false;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float* z = zz[h];
           float bmax = h ? bf16_hi(m2) : bf16_lo(m2);
-          if (a.rht_col) {
+          if (kRhtCol) {
             rht16(z, signs);
             bmax = 0.0f;
 #pragma unroll
@@ -337,8 +395,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
             if (kStash) {
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                w[i] = *reinterpret_cast<const uint32_t*>(stash + (16 * rb + i) * (kTN * 4) +
-                                                          swz_stash(cc >> 2) * 16 + (cc & 3) * 4);
+                w[i] = *reinterpret_cast<const uint32_t*>(stash + stash_off(16 * rb + i, cc));
             } else {
               const uint64_t base = a.ctr_off + (uint64_t)((R0 + 16 * rb) * N + C0 + cc);
 #pragma unroll
@@ -348,26 +405,35 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS) qu
               }
             }
           }
-          uint2 cd;
-          uint32_t e;
-          quant_block16<Q46, SR, SEL>(z, bmax, scC, w, cd, e);
-          codes[h] = cd;
-          es[h] = e;
+          quant_block16<Q46, SR, SEL, decltype(exact)::value>(z, bmax, scC, w, codes[h], es[h], redo);
         }
         tile::stage_col_pair(cstage, sstage, p, rb, codes[0], codes[1], es[0], es[1]);
+        return redo;
+      };
+      uint32_t redo = 0u;
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        const int rb = cp_rb0 + 2 * k;
+        if (16 * rb >= rows) break;
+        if (ctask(rb, std::false_type{})) redo |= 1u << k;
+      }
+      if (redo) {
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k)
+          if (redo & (1u << k)) ctask(cp_rb0 + 2 * k, std::true_type{});
       }
     }
-    __syncthreads();  // tile buffer free for the next prefetch; staging complete
+    __syncthreads();  // tile buffer free for the next copy; staging complete
     if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
   }
 }
 
-template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL, int RHT>
 cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   constexpr bool kStash = SR && ROW && COL;
-  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
+  constexpr int kSmem = (kStash ? 1 : 2) * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
                         (kStash ? kStashBytes : 0);
-  auto kern = quant1d_kernel<ROW, COL, Q46, SR, SEL>;
+  auto kern = quant1d_kernel<ROW, COL, Q46, SR, SEL, RHT>;
   // once per device: opt in to the dynamic shared memory and size the
   // persistent grid from the occupancy
   static int grid_cap[64] = {};
@@ -389,17 +455,33 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
   int64_t g = ntiles < cap ? ntiles : cap;
   if (g < 1) g = 1;
+  CUtensorMap xmap;
+  const cudaError_t me = make_tile_map(&xmap, a.x, a.M, a.N, a.ld);
+  if (me != cudaSuccess) return me;
   const dim3 grid((unsigned)g, 1, 1);
-  kern<<<grid, kBlockThreads, kSmem, s>>>(a);
+  kern<<<grid, kBlockThreads, kSmem, s>>>(a, xmap);
   return cudaGetLastError();
 }
 
-// All row/column/SR combinations of one (4/6, selection rule) pair.
+template <bool ROW, bool COL, bool Q46, int SEL, int RHT>
+cudaError_t launch_sr(const QuantArgs& a, bool sr, cudaStream_t s) {
+  return sr ? launch<ROW, COL, Q46, true, SEL, RHT>(a, s) : launch<ROW, COL, Q46, false, SEL, RHT>(a, s);
+}
+
+// All row/column/SR/RHT combinations of one (4/6, selection rule) pair.
 template <bool Q46, int SEL>
 cudaError_t launch_family(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s) {
-  if (row && col) return sr ? launch<true, true, Q46, true, SEL>(a, s) : launch<true, true, Q46, false, SEL>(a, s);
-  if (row) return sr ? launch<true, false, Q46, true, SEL>(a, s) : launch<true, false, Q46, false, SEL>(a, s);
-  return sr ? launch<false, true, Q46, true, SEL>(a, s) : launch<false, true, Q46, false, SEL>(a, s);
+  const int rht = (a.rht_row ? 1 : 0) | (a.rht_col ? 2 : 0);
+  if (row && col) {
+    switch (rht) {
+      case 0: return launch_sr<true, true, Q46, SEL, 0>(a, sr, s);
+      case 1: return launch_sr<true, true, Q46, SEL, 1>(a, sr, s);
+      case 2: return launch_sr<true, true, Q46, SEL, 2>(a, sr, s);
+      default: return launch_sr<true, true, Q46, SEL, 3>(a, sr, s);
+    }
+  }
+  if (row) return rht ? launch_sr<true, false, Q46, SEL, 1>(a, sr, s) : launch_sr<true, false, Q46, SEL, 0>(a, sr, s);
+  return rht ? launch_sr<false, true, Q46, SEL, 2>(a, sr, s) : launch_sr<false, true, Q46, SEL, 0>(a, sr, s);
 }
 
 }  // namespace q1d

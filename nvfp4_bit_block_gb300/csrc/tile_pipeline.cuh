@@ -1,12 +1,14 @@
-// tile_pipeline.cuh -- shared-memory tile streaming for the quantize kernels.
+// tile_pipeline.cuh -- shared-memory tile walk, staging and the cp.async
+// tile loader.
 //
-// Persistent CTAs walk the tensor in 64 x 256 bf16 tiles.  While a tile is
-// being quantized, the next one is already in flight: cp.async (16-byte
-// global -> shared copies, zero-filled outside the tensor) into the other of
-// two 32 KB buffers.  No thread ever spins: completion is cp.async.wait_group
-// plus __syncthreads.
+// Persistent CTAs walk the tensor in 64 x 256 bf16 tiles (Walker).  The 1D
+// quantize kernel fills its tiles with TMA (tma.cuh); the amax and 2D kernels
+// use the loader here: while a tile is being processed the next one is
+// already in flight as cp.async 16-byte global -> shared copies (zero-filled
+// outside the tensor) into the other of two 32 KB buffers, completed by
+// cp.async.wait_group plus __syncthreads.
 //
-// Shared tile layout: row r occupies 512 bytes; its 16-byte chunk c (eight
+// Loader tile layout: row r occupies 512 bytes; its 16-byte chunk c (eight
 // bf16 values) sits at chunk c ^ ((c >> 3) & 1).  Reading a row's 32-byte
 // block pair (chunks 2b, 2b+1) across 8 consecutive threads and reading one
 // 4-byte column-pair word across a warp are then both bank-conflict free.
@@ -89,6 +91,7 @@ __device__ __forceinline__ void load_async(uint8_t* buf, const uint16_t* x, int6
 
 __device__ __forceinline__ void commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_all_but_one() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // Two 16-byte chunks (16 bf16 values) of row r starting at tile column 16*b.
 __device__ __forceinline__ void read_row_block(const uint8_t* buf, int r, int b, uint32_t* wd) {

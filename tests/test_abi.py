@@ -53,7 +53,7 @@ def test_library_is_built_for_sm_103a_only():
 
 def test_strerror(L):
     assert nv.nvfp4_strerror(0) == "ok"
-    for st in (-1, -2, -3, -4, -5, -6, -7):
+    for st in (-1, -2, -3, -4, -5, -6, -7, -8):
         assert nv.nvfp4_strerror(st) not in ("", "unknown status")
     assert nv.nvfp4_strerror(12345) == "unknown status"
 

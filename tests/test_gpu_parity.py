@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
-Small cases span several CTA tiles (128 x 256) plus ragged tails and are
+Small cases span several CTA tiles (64 x 256) plus ragged tails and are
 compared element by element; the recipe's full-size workloads run in the
 launch configuration the benchmark times and are compared on sampled 16-row
 stripes that the oracle computes one by one.
@@ -139,6 +139,25 @@ def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
     assert g["status"] == -7
     st, am = oracle.amax(tiny, ROW)
     assert oracle.quantize(tiny, 32, am, ROW)["status"] == -7
+
+
+def test_tile_copy_timeout_is_reported_and_the_context_stays_usable():
+    """A 1D quantize whose tile copies never arrive (test hook: the tile
+    barrier is armed but no copy is issued) stops after its bounded wait and
+    reports NVFP4_ERR_PIPELINE in the status word; the next call on the same
+    context is correct."""
+    L = nv.lib()
+    hook = L.nvfp4_test_skip_next_copy
+    hook.restype = None
+    bits = synthetic.weight(64, 256, 3)  # a single tile
+    x = to_device(bits)
+    amax = nv.nvfp4_amax(x, ROW | COL)
+    hook()
+    out = nv.nvfp4_quantize(x, amax, ROW | COL)
+    torch.cuda.synchronize()
+    assert out.status.item() == -8
+    assert nv.nvfp4_strerror(-8).startswith("a tile copy")
+    assert_parity(gpu_quantize(x, ROW | COL), ref_quantize(bits, ROW | COL), ROW | COL)
 
 
 def test_two_d_copies_are_transposes_and_dequantize_identically():
