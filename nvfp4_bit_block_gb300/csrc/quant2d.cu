@@ -8,14 +8,20 @@
 // and 4 over all 256 elements ("Four Over Six (4/6)" technical summary,
 // Methodology).
 //
-// Persistent CTAs stream 64 x 256 tiles through double-buffered shared memory
-// (tile_pipeline.cuh).  Four threads share a 16x16 block, each holding 8 rows
-// x 8 columns: lane bit 0 picks the column half, lane bit 4 the row half, so
-// the block max and the 4/6 sums combine with two shuffles (xor 1, xor 16).
-// A warp covers 16 rows x 128 columns; the CTA's 8 warps cover the tile.
+// Persistent CTAs stream 64 x 256 tiles into double-buffered shared memory
+// with TMA (four 64 x 64 boxes, 128-byte swizzle, mbarrier completion with a
+// bounded wait), as the 1D kernel does.  Four threads share a 16x16 block,
+// each holding an 8 x 8 patch: lane bit 0 picks the column half, lane bit 4
+// the row half, so the block max and the 4/6 sums combine with two shuffles
+// (xor 1, xor 16).  A warp covers 16 rows x 128 columns; the CTA's 8 warps
+// cover the tile.  Each element is encoded once: a patch row's eight codes
+// are one rowwise word, and the columnwise bytes (two rows of one column)
+// come from interleaving the nibbles of two row words and a 4 x 4 byte
+// transpose.
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 #include "tile_pipeline.cuh"
+#include "tma.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -38,13 +44,18 @@ __device__ __forceinline__ float scaled(float z, const BlockScale& s, float Q, u
   return v;
 }
 
-// This thread's 8 values of row `lr` (0..7 within its row half).
-__device__ __forceinline__ void row8(const uint8_t* buf, int trow, int chunk, float* z) {
-  const uint4 q = *reinterpret_cast<const uint4*>(buf + trow * tile::kRowBytes + tile::swz(chunk) * 16);
-  z[0] = bf16_lo(q.x); z[1] = bf16_hi(q.x);
-  z[2] = bf16_lo(q.y); z[3] = bf16_hi(q.y);
-  z[4] = bf16_lo(q.z); z[5] = bf16_hi(q.z);
-  z[6] = bf16_lo(q.w); z[7] = bf16_hi(q.w);
+// Row i (0..7) of this thread's 8 x 8 patch as eight floats.  `pbase` is the
+// patch's box plus its first row (a multiple of 8), so with the 128-byte
+// swizzle the patch's chunk c of row i sits at (c ^ i) * 16.
+__device__ __forceinline__ void patch_row(const uint8_t* pbase, int c, int i, float* z) {
+  const uint4 q = *reinterpret_cast<const uint4*>(pbase + i * 128 + ((c ^ i) << 4));
+  const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = bf16x2_to_f32x2(wd[k]);
+    z[2 * k] = f.x;
+    z[2 * k + 1] = f.y;
+  }
 }
 
 // 4/6 score of the 16x16 block at scale s: per row a tree over this lane's 8
@@ -52,13 +63,13 @@ __device__ __forceinline__ void row8(const uint8_t* buf, int trow, int chunk, fl
 // then the two row halves.  Same order as a perfect binary tree over the 256
 // elements in row-major order.
 template <bool SR>
-__device__ __forceinline__ float block_score(const uint8_t* buf, int trow0, int chunk, const BlockScale& s,
-                                             float Q, const QuantArgs& a, int64_t grow0, int64_t gcol0, int sel) {
+__device__ __forceinline__ float block_score(const uint8_t* pbase, int c, const BlockScale& s, float Q,
+                                             const QuantArgs& a, int64_t grow0, int64_t gcol0, int sel) {
   float rows[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     float z[8], v[8];
-    row8(buf, trow0 + i, chunk, z);
+    patch_row(pbase, c, i, z);
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = scaled<SR>(z[j], s, Q, SR ? word0_of(a, grow0 + i, gcol0 + j) : 0u);
     const float part = score8(z, e2m1x8(v), s.d, sel);
@@ -70,116 +81,176 @@ __device__ __forceinline__ float block_score(const uint8_t* buf, int trow0, int 
   return err_combine(h, __shfl_xor_sync(0xFFFFFFFFu, h, 16), sel);
 }
 
+// Byte m of each of w[0..3] gathered into output word m (a 4 x 4 byte transpose).
+__device__ __forceinline__ void transpose4x4(const uint32_t* w, uint32_t* t) {
+  const uint32_t a_lo = __byte_perm(w[0], w[1], 0x5140), a_hi = __byte_perm(w[0], w[1], 0x7362);
+  const uint32_t b_lo = __byte_perm(w[2], w[3], 0x5140), b_hi = __byte_perm(w[2], w[3], 0x7362);
+  t[0] = __byte_perm(a_lo, b_lo, 0x5410);
+  t[1] = __byte_perm(a_lo, b_lo, 0x7632);
+  t[2] = __byte_perm(a_hi, b_hi, 0x5410);
+  t[3] = __byte_perm(a_hi, b_hi, 0x7632);
+}
+
 template <bool ROW, bool COL, bool Q46, bool SR>
-__global__ void __launch_bounds__(kBlockThreads) quant2d_kernel(const QuantArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* bufs = smem;
+__global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) ? 2 : 3))
+    quant2d_kernel(const QuantArgs a, const __grid_constant__ CUtensorMap xmap) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* bufs = smem;                                  // 2 x 32 KB tiles (1024-aligned)
   uint8_t* cstage = smem + 2 * tile::kTileBytes;
   uint8_t* sstage = cstage + tile::kCStageBytes;
+  const uint32_t bar0 = tile::smem_u32(sstage + tile::kSStageBytes), bar1 = bar0 + 8;
 
   const float den = Q46 ? kAlphaDen46 : kAlphaDen;
   const float A = a.amax[0];
   const float alpha = __fdiv_rn(A, den);
   const int st = amax_status(A);
+  const bool misaligned = (tile::smem_u32(smem) & 1023u) != 0u;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.alpha[0] = alpha;
     a.alpha[1] = __fdiv_rn(a.amax[1], den);
     if (st && a.status) *a.status = st;
+    if (misaligned && !st && a.status) *a.status = kStatusPipeline;
   }
-  if (st) return;
+  if (st || misaligned) return;
 
   const int64_t M = a.M, N = a.N;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ch = lane & 1, bcol = (lane >> 1) & 7, rh = lane >> 4;
   const int rb = warp >> 1;                                // row block of this warp
   const int tcol0 = 128 * (warp & 1) + 16 * bcol + 8 * ch; // first tile column of this thread
-  const int chunk = tcol0 >> 3;
   const int trow0 = 16 * rb + 8 * rh;                      // first tile row of this thread
+  const int pc = (tcol0 & 63) >> 3;                        // the patch's 16-byte chunk within its box
+  const uint32_t poff = (tcol0 >> 6) * 8192 + trow0 * 128; // the patch's box and first row
+  const int64_t hN = N / 2, sN = N / 16;
+  if (tid == 0) {
+    tma::mbar_init(bar0, 1);
+    tma::mbar_init(bar1, 1);
+    tma::fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int b, const tile::Coord& c) {
+    const uint32_t bar = b ? bar1 : bar0;
+    tma::arrive_expect_tx(bar, tile::kTileBytes);
+    const uint32_t dst = tile::smem_u32(bufs + b * tile::kTileBytes);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
+  };
 
   tile::Walker w;
   w.init(M, N);
-  if (w.valid()) tile::load_async<kBlockThreads>(bufs, a.x, M, N, a.ld, w.coord(), tid);
-  tile::commit();
+  if (tid == 0 && w.valid()) issue(0, w.coord());
   for (int it = 0; w.valid(); w = w.next(), ++it) {
-    uint8_t* buf = bufs + (it & 1) * tile::kTileBytes;
-    const tile::Walker wn = w.next();
-    if (wn.valid())
-      tile::load_async<kBlockThreads>(bufs + ((it + 1) & 1) * tile::kTileBytes, a.x, M, N, a.ld, wn.coord(), tid);
-    tile::commit();
-    tile::wait_all_but_one();
-    __syncthreads();
+    const int b = it & 1;
+    const uint8_t* buf = bufs + b * tile::kTileBytes;
+    if (tid == 0) {
+      const tile::Walker wn = w.next();
+      if (wn.valid()) issue(b ^ 1, wn.coord());  // that buffer was released by the last barrier
+    }
+    const uint32_t parity = (it >> 1) & 1;
+    const bool arrived = tma::wait(b ? bar1 : bar0, parity);
+    if (!__syncthreads_and(arrived)) {
+      if (tid == 0) {
+        if (a.status) atomicExch(a.status, kStatusPipeline);
+        tma::wait(b ? bar1 : bar0, parity);
+        if (w.next().valid()) tma::wait(b ? bar0 : bar1, ((it + 1) >> 1) & 1);
+      }
+      return;
+    }
     const tile::Coord tc = w.coord();
     const int64_t grow0 = tc.R0 + trow0, gcol0 = tc.C0 + tcol0;
     // a block is valid when its 16 rows and 16 columns lie inside the tensor
     const bool valid = (tc.R0 + 16 * rb < M) && (tc.C0 + (tcol0 & ~15) < N);
+    const uint8_t* pbase = buf + poff;
 
     // a5: block maximum over 256 values
     uint32_t m2 = 0u;
-#pragma unroll 1
+#pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint4 q = *reinterpret_cast<const uint4*>(buf + (trow0 + i) * tile::kRowBytes + tile::swz(chunk) * 16);
+      const uint4 q = *reinterpret_cast<const uint4*>(pbase + i * 128 + ((pc ^ i) << 4));
       m2 = absmax_bf16x2(m2, absmax_bf16x2(absmax_bf16x2(q.x, q.y), absmax_bf16x2(q.z, q.w)));
     }
     m2 &= 0x7FFF7FFFu;
-    float b = fmaxf(bf16_lo(m2), bf16_hi(m2));
-    b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
-    b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 16));
+    float bmax = fmaxf(bf16_lo(m2), bf16_hi(m2));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 16));
 
-    BlockScale s = block_scale(b, alpha, 6.0f);
+    BlockScale s = block_scale(bmax, alpha, 6.0f);
     float Q = 6.0f;
     if (Q46) {
-      const BlockScale s4 = block_scale(b, alpha, 4.0f);
-      const float sc6 = block_score<SR>(buf, trow0, chunk, s, 6.0f, a, grow0, gcol0, a.sel);
-      const float sc4 = block_score<SR>(buf, trow0, chunk, s4, 4.0f, a, grow0, gcol0, a.sel);
+      const BlockScale s4 = block_scale(bmax, alpha, 4.0f);
+      const float sc6 = block_score<SR>(pbase, pc, s, 6.0f, a, grow0, gcol0, a.sel);
+      const float sc4 = block_score<SR>(pbase, pc, s4, 4.0f, a, grow0, gcol0, a.sel);
       if (sc4 < sc6) {
         s = s4;
         Q = 4.0f;
       }
     }
+    const bool clamp = !SR && Q == 4.0f && s.e < 8u;  // RN at a subnormal max-4 scale
 
-    // a7 + a9: each element once, packed rowwise (pairs along a row, stored
-    // directly) and columnwise (pairs along a column, staged)
-    uint32_t cq[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll 1
-    for (int i = 0; i < 8; i += 2) {
-      float z0[8], z1[8], v0[8], v1[8];
-      row8(buf, trow0 + i, chunk, z0);
-      row8(buf, trow0 + i + 1, chunk, z1);
+    // a7 + a9: each element encoded once; rows of codes go to R directly,
+    // and pairs of rows become C bytes
+    uint32_t lo[4], hi[4];
+    uint8_t* qr = a.q_row + grow0 * hN + gcol0 / 2;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v0[j] = scaled<SR>(z0[j], s, Q, SR ? word0_of(a, grow0 + i, gcol0 + j) : 0u);
-        v1[j] = scaled<SR>(z1[j], s, Q, SR ? word0_of(a, grow0 + i + 1, gcol0 + j) : 0u);
-      }
-      if (ROW && valid) {
-        *reinterpret_cast<uint32_t*>(a.q_row + (grow0 + i) * (N / 2) + gcol0 / 2) = e2m1x8(v0);
-        *reinterpret_cast<uint32_t*>(a.q_row + (grow0 + i + 1) * (N / 2) + gcol0 / 2) = e2m1x8(v1);
-      }
-      if (COL) {
+    for (int p2 = 0; p2 < 4; ++p2) {
+      uint32_t code[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cq[j] |= e2m1x2(v0[j], v1[j]) << (4 * i);
+      for (int h = 0; h < 2; ++h) {
+        const int i = 2 * p2 + h;
+        float z[8], v[8];
+        patch_row(pbase, pc, i, z);
+        if (SR) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = scaled<true>(z[j], s, Q, word0_of(a, grow0 + i, gcol0 + j));
+        } else {
+          const float2 inv2 = make_float2(s.inv, s.inv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
+            v[2 * j] = r.x;
+            v[2 * j + 1] = r.y;
+          }
+          if (clamp) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
+          }
+        }
+        code[h] = e2m1x8(v);
+        if (ROW && valid) *reinterpret_cast<uint32_t*>(qr + i * hN) = code[h];
       }
+      // column j = 2m: byte m of lo; j = 2m+1: byte m of hi (row i low nibble)
+      lo[p2] = (code[0] & 0x0F0F0F0Fu) | ((code[1] & 0x0F0F0F0Fu) << 4);
+      hi[p2] = ((code[0] >> 4) & 0x0F0F0F0Fu) | (code[1] & 0xF0F0F0F0u);
     }
     if (COL) {
+      uint32_t tl[4], th[4];
+      transpose4x4(lo, tl);
+      transpose4x4(hi, th);
+      uint8_t* cs = cstage + rb * (kTN * 8) + tcol0 * 8 + 4 * rh;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint32_t*>(cstage + rb * (kTN * 8) + (tcol0 + j) * 8 + 4 * rh) = cq[j];
+      for (int m = 0; m < 4; ++m) {
+        *reinterpret_cast<uint32_t*>(cs + (2 * m) * 8) = tl[m];
+        *reinterpret_cast<uint32_t*>(cs + (2 * m + 1) * 8) = th[m];
+      }
       if (rh == 0) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) sstage[(tcol0 + j) * 4 + rb] = (uint8_t)s.e;
       }
     }
     if (ROW && valid && ch == 0) {
+      uint8_t* sr = a.s_row + grow0 * sN + gcol0 / 16;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a.s_row[(grow0 + i) * (N / 16) + gcol0 / 16] = (uint8_t)s.e;
+      for (int i = 0; i < 8; ++i) sr[i * sN] = (uint8_t)s.e;
     }
-    __syncthreads();
+    __syncthreads();  // tile buffer free for the next copy; staging complete
     if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
   }
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR>
 cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
-  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes;
+  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 16;  // + 2 barriers
   auto kern = quant2d_kernel<ROW, COL, Q46, SR>;
   static int grid_cap[64] = {};
   int dev = 0;
@@ -199,7 +270,10 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
   const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
   int64_t grid = ntiles < cap ? ntiles : cap;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kBlockThreads, kSmem, st>>>(a);
+  CUtensorMap xmap;
+  const cudaError_t me = make_tile_map(&xmap, a.x, a.M, a.N, a.ld);
+  if (me != cudaSuccess) return me;
+  kern<<<(unsigned)grid, kBlockThreads, kSmem, st>>>(a, xmap);
   return cudaGetLastError();
 }
 
