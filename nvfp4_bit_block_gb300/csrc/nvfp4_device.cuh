@@ -225,24 +225,25 @@ __device__ __forceinline__ BlockScale block_scale(float b, float alpha, float Q)
   return s;
 }
 
-// Scale byte of a block: e = E4M3(fl(b / den)).  The quotient is taken as
-// b * (1/den), which is within 2 ulp of fl(b / den); the two give the same
-// E4M3 byte unless an E4M3 rounding midpoint (fp32 bits 19..0 == 0x80000 in
-// the normal range) lies within 3 ulp, or the value is in E4M3's subnormal
-// range.  Such blocks (a few in a million) are flagged in `exact_needed` and
-// redone by the caller with the IEEE division (scale_byte_exact); keeping
-// that division out of the main path leaves it free of branches.
-// rden = 1/den, correctly rounded.
-__device__ __forceinline__ uint32_t scale_byte_fast(float b, float rden, bool& exact_needed) {
-  const float t = __fmul_rn(b, rden);
-  const uint32_t u = __float_as_uint(t);
-  // bits 19..0 of t within [0x7FFFD, 0x80004], or 0 < t < 2^-6 (t >= 0 here)
-  exact_needed = exact_needed || ((u + 3u) & 0xFFFF8u) == 0x80000u || u - 1u < 0x3C7FFFFFu;
-  return e4m3_encode(t);  // b == 0 gives t == 0 and byte 0
+// fl(b / den), the correctly rounded quotient, from rden = fl(1/den) without
+// a division: q0 = fl(b * rden) is within 2 ulp of b / den, and each residual
+// correction q' = q + (b - q*den) * rden (fused multiply-adds; the residual
+// of a close quotient is exact) brings it closer; after two of them the
+// result is fl(b / den) -- Markstein's correction theorem once the first
+// step has made q faithful.  Checked against the IEEE division for every
+// pair of a bf16 block maximum and a bf16 tensor amax (see selftest.cu).
+// b >= 0 finite, den > 0 normal, or den == rden == 0 with b == 0.
+__device__ __forceinline__ float quotient_rn(float b, float den, float rden) {
+  float q = __fmul_rn(b, rden);
+  float r = __fmaf_rn(-q, den, b);
+  q = __fmaf_rn(r, rden, q);
+  r = __fmaf_rn(-q, den, b);
+  return __fmaf_rn(r, rden, q);
 }
 
-__device__ __forceinline__ uint32_t scale_byte_exact(float b, float den) {
-  return (b > 0.0f) ? e4m3_encode(__fdiv_rn(b, den)) : 0u;
+// Scale byte of a block: e = E4M3(fl(b / den)), den = Q * alpha.
+__device__ __forceinline__ uint32_t scale_byte(float b, float den, float rden) {
+  return e4m3_encode(quotient_rn(b, den, rden));  // b == 0 gives byte 0
 }
 
 // Per-copy table of d = e*alpha and 1/d for every scale byte e (0..127),

@@ -26,8 +26,6 @@
 #include "tile_pipeline.cuh"
 #include "tma.cuh"
 
-#include <type_traits>
-
 #ifndef NVFP4_Q1D_MIN_CTAS
 #define NVFP4_Q1D_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for
 #endif
@@ -147,14 +145,12 @@ __device__ __forceinline__ float candidate16(const float* z, uint32_t e, float2 
   return __fadd_rn(c.x, c.y);
 }
 
-// One block: the standard max-6 candidate and, with 4/6, the max-4 candidate;
-// the max-4 one is kept only if its score is strictly lower.
-// EXACT = false: scale bytes from the fast product, `redo` set when the
-// block needs the IEEE division; EXACT = true: the division itself.
-template <bool Q46, bool SR, int SEL, bool EXACT>
-__device__ __forceinline__ void quant_block16(const float* z, float bmax, const CopyScales& sc, const uint32_t* w,
-                                              uint2& codes, uint32_t& e, bool& redo) {
-  const uint32_t e6 = EXACT ? scale_byte_exact(bmax, sc.den6) : scale_byte_fast(bmax, sc.rden6, redo);
+// One block at the given scale bytes: the standard max-6 candidate and, with
+// 4/6, the max-4 candidate; the max-4 one is kept only if its score is
+// strictly lower.
+template <bool Q46, bool SR, int SEL>
+__device__ __forceinline__ void quant_block16(const float* z, const CopyScales& sc, const uint32_t* w, uint32_t e6,
+                                              uint32_t e4, uint2& codes, uint32_t& e) {
   const float2 di6 = sc.tbl[e6];
   if (!Q46) {
     float v[16];
@@ -165,11 +161,17 @@ __device__ __forceinline__ void quant_block16(const float* z, float bmax, const 
   }
   uint2 c6, c4;
   const float s6 = candidate16<SR, SEL>(z, e6, di6, 6.0f, w, c6);
-  const uint32_t e4 = EXACT ? scale_byte_exact(bmax, sc.den4) : scale_byte_fast(bmax, sc.rden4, redo);
   const float s4 = candidate16<SR, SEL>(z, e4, sc.tbl[e4], 4.0f, w, c4);
   const bool four = s4 < s6;
   codes = four ? c4 : c6;
   e = four ? e4 : e6;
+}
+
+// Scale bytes of a block with maximum b (e4 only with 4/6).
+template <bool Q46>
+__device__ __forceinline__ void block_bytes(float b, const CopyScales& sc, uint32_t& e6, uint32_t& e4) {
+  e6 = scale_byte(b, sc.den6, sc.rden6);
+  e4 = Q46 ? scale_byte(b, sc.den4, sc.rden4) : 0u;
 }
 
 // RHT bit 0: Hadamard on the rowwise copy; bit 1: on the columnwise copy.
@@ -284,8 +286,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
       uint8_t* qt = a.q_row + (R0 + rr) * hN + C0 / 2 + 8 * rq;
       uint8_t* st = a.s_row + (R0 + rr) * sN + C0 / 16 + rq;
       const uint64_t ct = a.ctr_off + (uint64_t)((R0 + rr) * N + C0 + 16 * rq);
-      // block rq + 4k of row rr; returns whether the block needs the exact scale path
-      auto rblock = [&](int k, auto exact) -> bool {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // block rq + 4k of row rr
+        if (16 * (rq + 4 * k) >= cols) break;
         uint32_t wd[8];
         {
           const uint4 lo = *reinterpret_cast<const uint4*>(buf + k * 8192 + r_chunk0);
@@ -309,6 +312,8 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
         } else {
           bmax = block_absmax16(wd);
         }
+        uint32_t e6, e4;
+        block_bytes<Q46>(bmax, scR, e6, e4);
         uint32_t w[16];
         if (SR) {
           const uint64_t base = ct + (uint64_t)(64 * k);
@@ -329,22 +334,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
         }
         uint2 codes;
         uint32_t e;
-        bool redo = false;
-        quant_block16<Q46, SR, SEL, decltype(exact)::value>(z, bmax, scR, w, codes, e, redo);
+        quant_block16<Q46, SR, SEL>(z, scR, w, e6, e4, codes, e);
         *reinterpret_cast<uint2*>(qt + 32 * k) = codes;
         st[4 * k] = (uint8_t)e;
-        return redo;
-      };
-      uint32_t redo = 0u;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (16 * (rq + 4 * k) >= cols) break;
-        if (rblock(k, std::false_type{})) redo |= 1u << k;
-      }
-      if (redo) {  // rare: redo those blocks with the exact scale bytes
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k)
-          if (redo & (1u << k)) rblock(k, std::true_type{});
       }
     }
     if (kStash) __syncthreads();
@@ -352,8 +344,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
     if (COL && cp_ok) {
       const int p = cp_p;
-      // row block rb of column pair p; returns whether a block needs the exact scale path
-      auto ctask = [&](int rb, auto exact) -> bool {
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {  // row block rb of column pair p (both columns)
+        const int rb = cp_rb0 + 2 * k;
+        if (16 * rb >= rows) break;
         uint32_t wd[16];
         const uint8_t* cb = buf + c_base + rb * 2048;
 #pragma unroll
@@ -369,8 +363,6 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
                              absmax_bf16x2(absmax_bf16x2(t8[4], t8[5]), absmax_bf16x2(t8[6], t8[7]))) &
                0x7FFF7FFFu;
         }
-        uint2 codes[2];
-        uint32_t es[2];
         float zz[2][16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -378,17 +370,24 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
           zz[0][i] = f.x;
           zz[1][i] = f.y;
         }
-        bool redo = false;
+        float bm[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float* z = zz[h];
-          float bmax = h ? bf16_hi(m2) : bf16_lo(m2);
+          bm[h] = h ? bf16_hi(m2) : bf16_lo(m2);
           if (kRhtCol) {
-            rht16(z, signs);
-            bmax = 0.0f;
+            rht16(zz[h], signs);
+            bm[h] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(z[i]));
+            for (int i = 0; i < 16; ++i) bm[h] = fmaxf(bm[h], fabsf(zz[h][i]));
           }
+        }
+        uint32_t e6[2], e4[2];
+        block_bytes<Q46>(bm[0], scC, e6[0], e4[0]);
+        block_bytes<Q46>(bm[1], scC, e6[1], e4[1]);
+        uint2 codes[2];
+        uint32_t es[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
           const int cc = 2 * p + h;  // tile column
           uint32_t w[16];
           if (SR) {
@@ -405,22 +404,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
               }
             }
           }
-          quant_block16<Q46, SR, SEL, decltype(exact)::value>(z, bmax, scC, w, codes[h], es[h], redo);
+          quant_block16<Q46, SR, SEL>(zz[h], scC, w, e6[h], e4[h], codes[h], es[h]);
         }
         tile::stage_col_pair(cstage, sstage, p, rb, codes[0], codes[1], es[0], es[1]);
-        return redo;
-      };
-      uint32_t redo = 0u;
-#pragma unroll 1
-      for (int k = 0; k < 2; ++k) {
-        const int rb = cp_rb0 + 2 * k;
-        if (16 * rb >= rows) break;
-        if (ctask(rb, std::false_type{})) redo |= 1u << k;
-      }
-      if (redo) {
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k)
-          if (redo & (1u << k)) ctask(cp_rb0 + 2 * k, std::true_type{});
       }
     }
     __syncthreads();  // tile buffer free for the next copy; staging complete

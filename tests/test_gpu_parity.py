@@ -141,6 +141,27 @@ def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
     assert oracle.quantize(tiny, 32, am, ROW)["status"] == -7
 
 
+def test_scale_quotient_equals_ieee_division_exhaustively():
+    """The kernels form each scale byte from a division-free quotient (a
+    product and two residual corrections).  For every bf16 block maximum
+    b <= every accepted bf16 amax A (and 256 random fp32 maxima per A, as
+    Hadamard-transformed blocks have), at Q = 6 over 6*448 and Q = 6, 4 over
+    6*256: its E4M3 byte equals the byte of the IEEE quotient, and the
+    quotient itself is the IEEE quotient wherever that is a normal fp32
+    number (below 2^-126 the byte is 0 either way)."""
+    import ctypes
+    L = nv.lib()
+    f = L.nvfp4_test_quotient_check
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    out = torch.zeros(6, dtype=torch.int64, device="cuda")
+    assert f(out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    bytes_differ, _normal_quotients_differ, first, _quotients_differ, _one_step, bare = out.tolist()
+    assert bytes_differ == 0, hex(first)
+    assert bare > 0  # the bare product b * (1/den) alone is not enough
+
+
 def test_tile_copy_timeout_is_reported_and_the_context_stays_usable():
     """A 1D quantize whose tile copies never arrive (test hook: the tile
     barrier is armed but no copy is issued) stops after its bounded wait and
