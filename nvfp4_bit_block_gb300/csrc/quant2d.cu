@@ -96,9 +96,9 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
     quant2d_kernel(const QuantArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* bufs = smem;                                  // 2 x 32 KB tiles (1024-aligned)
-  uint8_t* cstage = smem + 2 * tile::kTileBytes;
-  uint8_t* sstage = cstage + tile::kCStageBytes;
-  const uint32_t bar0 = tile::smem_u32(sstage + tile::kSStageBytes), bar1 = bar0 + 8;
+  uint8_t* cstage = smem + 2 * tile::kTileBytes;  // padded layouts (lanes hold columns 8 apart)
+  uint8_t* sstage = cstage + tile::kCStagePadBytes;
+  const uint32_t bar0 = tile::smem_u32(sstage + tile::kSStagePadBytes), bar1 = bar0 + 8;
 
   const float den = Q46 ? kAlphaDen46 : kAlphaDen;
   const float A = a.amax[0];
@@ -227,15 +227,17 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
       uint32_t tl[4], th[4];
       transpose4x4(lo, tl);
       transpose4x4(hi, th);
-      uint8_t* cs = cstage + rb * (kTN * 8) + tcol0 * 8 + 4 * rh;
+      // the thread's 8 columns lie inside one 16-column group: one pad offset
+      uint8_t* cs = cstage + tile::cstage_off_pad(rb, tcol0) + 4 * rh;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         *reinterpret_cast<uint32_t*>(cs + (2 * m) * 8) = tl[m];
         *reinterpret_cast<uint32_t*>(cs + (2 * m + 1) * 8) = th[m];
       }
       if (rh == 0) {
+        uint8_t* ss = sstage + tile::sstage_off_pad(tcol0) + rb;  // 8 columns, one 8-column group
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sstage[(tcol0 + j) * 4 + rb] = (uint8_t)s.e;
+        for (int j = 0; j < 8; ++j) ss[4 * j] = (uint8_t)s.e;
       }
     }
     if (ROW && valid && ch == 0) {
@@ -244,13 +246,13 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
       for (int i = 0; i < 8; ++i) sr[i * sN] = (uint8_t)s.e;
     }
     __syncthreads();  // tile buffer free for the next copy; staging complete
-    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
+    if (COL) tile::write_col_outputs<true>(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
   }
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR>
 cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
-  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 16;  // + 2 barriers
+  constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStagePadBytes + tile::kSStagePadBytes + 16;  // + 2 barriers
   auto kern = quant2d_kernel<ROW, COL, Q46, SR>;
   static int grid_cap[64] = {};
   int dev = 0;

@@ -120,8 +120,18 @@ __device__ __forceinline__ void st_v8(uint8_t* p, uint2 a, uint2 b, uint2 c, uin
                : "memory");
 }
 
+// Padded staging (PAD = true) for writers whose lanes hold columns 8 apart:
+// 16 bytes after every 16 columns of codes and 4 bytes after every 8 columns
+// of scales spread such lanes over all banks.
+constexpr int kCStageRowPad = kTN * 8 + (kTN / 16) * 16;          // 2304 bytes per row block
+constexpr int kCStagePadBytes = 4 * kCStageRowPad;                // 9 KB
+constexpr int kSStagePadBytes = kTN * 4 + (kTN / 8) * 4;          // 1152 bytes
+__device__ __forceinline__ int cstage_off_pad(int rb, int c) { return rb * kCStageRowPad + 8 * c + 16 * (c >> 4); }
+__device__ __forceinline__ int sstage_off_pad(int c) { return 4 * c + 4 * (c >> 3); }
+
 // Write the staged columnwise outputs of one tile: tile column `c` (one per
 // thread) gets its codes for up to 64 rows (32 bytes) and up to 4 scales.
+template <bool PAD = false>
 __device__ __forceinline__ void write_col_outputs(const uint8_t* cstage, const uint8_t* sstage, uint8_t* q_col,
                                                   uint8_t* s_col, int64_t M, int64_t N, Coord tc, int c) {
   const int64_t gc = tc.C0 + c;
@@ -130,7 +140,8 @@ __device__ __forceinline__ void write_col_outputs(const uint8_t* cstage, const u
   if (nrb > 4) nrb = 4;
   uint2 w[4];
 #pragma unroll
-  for (int rb = 0; rb < 4; ++rb) w[rb] = *reinterpret_cast<const uint2*>(cstage + rb * (kTN * 8) + c * 8);
+  for (int rb = 0; rb < 4; ++rb)
+    w[rb] = *reinterpret_cast<const uint2*>(cstage + (PAD ? cstage_off_pad(rb, c) : rb * (kTN * 8) + c * 8));
   uint8_t* dst = q_col + gc * (M / 2) + tc.R0 / 2;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(dst);
   if (nrb == 4 && (addr & 31) == 0) {
@@ -141,7 +152,7 @@ __device__ __forceinline__ void write_col_outputs(const uint8_t* cstage, const u
   } else {
     for (int rb = 0; rb < nrb; ++rb) *reinterpret_cast<uint2*>(dst + 8 * rb) = w[rb];
   }
-  const uint32_t sw = *reinterpret_cast<const uint32_t*>(sstage + c * 4);
+  const uint32_t sw = *reinterpret_cast<const uint32_t*>(sstage + (PAD ? sstage_off_pad(c) : c * 4));
   uint8_t* sdst = s_col + gc * (M / 16) + tc.R0 / 16;
   if (nrb == 4 && (reinterpret_cast<uintptr_t>(sdst) & 3) == 0) {
     *reinterpret_cast<uint32_t*>(sdst) = sw;
