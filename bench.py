@@ -39,6 +39,14 @@ METRIC = "NVFP4 quantize GB/s (bf16 in + fp4/scales out), % of GB300 HBM peak"
 UNIT = "GB/s"
 
 
+# DRAM bytes (read + written) of one quantize launch, from one ncu capture of
+# the current kernel on that workload (cold cache; outputs partly still in L2
+# at kernel end).  Keyed by (workload, flags, selection); absent -> null.
+QUANTIZE_TRAFFIC_BYTES = {
+    ("act_46mae_8192x5120", 67, 0): 83_943_680 + 9_834_752,
+}
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """The largest `value` over all ranks (the slowest rank sets the job time)."""
     if world <= 1:
@@ -264,7 +272,8 @@ def run_ours(args, rank: int, world: int):
         "kernels_ms": {"amax": round(statistics.mean(amax_ms), 5), "quantize": round(quant_avg_ms, 5)},
         "elements_per_s": round(M * N * args.steps * world / (total_ms * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": QUANTIZE_TRAFFIC_BYTES.get((args.workload, flags, sel)), "peak_kind": peak_kind,
                      "kernel": "quantize"},
         "step_frac_of_peak": round(value / world / peak, 4),
         "e2e": {"value": round(nbytes / e2e_s / 1e9 * world, 1), "unit": UNIT,
