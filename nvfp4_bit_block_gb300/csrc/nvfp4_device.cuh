@@ -241,10 +241,20 @@ __device__ __forceinline__ float quotient_rn(float b, float den, float rden) {
   return __fmaf_rn(r, rden, q);
 }
 
-// Scale byte of a block: e = E4M3(fl(b / den)), den = Q * alpha.
+// Scale byte of a block: e = E4M3(fl(b / den)), den = Q * alpha.  Every
+// quotient from 464 up saturates to 448 (byte 0x7E); the cap keeps the
+// corrections from turning an overflowing quotient (b >> amax, possible with a
+// caller-supplied amax) into NaN, whose byte would be 0x7F.
 __device__ __forceinline__ uint32_t scale_byte(float b, float den, float rden) {
-  return e4m3_encode(quotient_rn(b, den, rden));  // b == 0 gives byte 0
+  return e4m3_encode(fminf(quotient_rn(b, den, rden), 1.0e6f));  // b == 0 gives byte 0
 }
+
+// A max-4 candidate needs its scaled values clamped to +-4 before rounding to
+// nearest only when its scale byte is subnormal (< 8: E4M3 rounding error up
+// to 50 %) or saturated (0x7E: the block maximum may exceed 448 * 4 * alpha,
+// e.g. with a caller-supplied amax); otherwise every scaled value is at most
+// 4.25 and rounds to at most 4.
+__device__ __forceinline__ bool max4_needs_clamp(uint32_t e) { return e < 8u || e >= 0x7Eu; }
 
 // Per-copy table of d = e*alpha and 1/d for every scale byte e (0..127),
 // filled once per CTA: entry e = (d, inv) exactly as block_scale computes them.

@@ -81,7 +81,7 @@ __device__ __forceinline__ void scale16(const float* z, float inv, uint32_t e, f
   if (SR) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = sr_round(v[j], Q, w[j]);
-  } else if (Q == 4.0f && e < 8u) {
+  } else if (Q == 4.0f && max4_needs_clamp(e)) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
   }
@@ -98,7 +98,7 @@ __device__ __forceinline__ float candidate16(const float* z, uint32_t e, float2 
                                              uint2& codes) {
   const float2 inv2 = make_float2(di.y, di.y);
   const float2 nd = make_float2(-di.x, -di.x);
-  const bool clamp = !SR && Q == 4.0f && e < 8u;
+  const bool clamp = !SR && Q == 4.0f && max4_needs_clamp(e);
   float t[8];
   uint32_t cw[2];
 #pragma unroll

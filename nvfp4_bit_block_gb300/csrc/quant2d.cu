@@ -40,7 +40,7 @@ template <bool SR>
 __device__ __forceinline__ float scaled(float z, const BlockScale& s, float Q, uint32_t w) {
   float v = __fmul_rn(z, s.inv);
   if (SR) return sr_round(v, Q, w);
-  if (Q == 4.0f && s.e < 8u) v = fminf(fmaxf(v, -4.0f), 4.0f);
+  if (Q == 4.0f && max4_needs_clamp(s.e)) v = fminf(fmaxf(v, -4.0f), 4.0f);
   return v;
 }
 
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
         Q = 4.0f;
       }
     }
-    const bool clamp = !SR && Q == 4.0f && s.e < 8u;  // RN at a subnormal max-4 scale
+    const bool clamp = !SR && Q == 4.0f && max4_needs_clamp(s.e);  // RN at a subnormal or saturated max-4 scale
 
     // a7 + a9: each element encoded once; rows of codes go to R directly,
     // and pairs of rows become C bytes

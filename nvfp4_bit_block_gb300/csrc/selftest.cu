@@ -1,16 +1,18 @@
 // selftest.cu -- exhaustive device check of the scale-byte quotient.
 //
-// The quantize kernels take E4M3(fl(b / den)) from quotient_rn (a product
-// and two residual corrections) instead of an IEEE division.  This kernel
-// compares the two for every pair of a bf16 block maximum b and a bf16 tensor
-// amax A that the library accepts (2^-100 <= A finite, 0 <= b <= A), with
-// den = Q * (A / 2688) for Q = 6 and den = Q * (A / 1536) for Q = 6 and 4,
-// exactly as the kernels form them; plus 256 pseudo-random fp32 maxima per
-// (A, den) as a transformed (Hadamard) block has.  It reports how many scale
-// bytes differ, how many quotients differ where the IEEE quotient is a normal
-// fp32 number (the corrections are exact there), how many differ at all (in
-// the fp32 subnormal range the residuals underflow; every byte there is 0),
-// and the first differing byte case.
+// The quantize kernels take E4M3(fl(b / den)) from scale_byte (quotient_rn:
+// a product and two residual corrections, capped at 1e6) instead of an IEEE
+// division.  This kernel compares the two bytes for every pair of a bf16
+// block maximum b (any finite value: an amax supplied by the caller may be
+// smaller than the block) and a bf16 tensor amax A that the library accepts
+// (2^-100 <= A finite), with den = Q * (A / 2688) for Q = 6 and
+// den = Q * (A / 1536) for Q = 6 and 4, exactly as the kernels form them; the
+// same again with A replaced by a pseudo-random fp32 value just above it (an
+// amax that is not a bf16 value, e.g. of a transformed copy); and 256
+// pseudo-random fp32 maxima in [0, 4A) per (A, den), as a transformed
+// (Hadamard) block has.  It reports how many scale bytes differ, how many
+// quotients differ where the IEEE quotient is a normal fp32 number below the
+// cap, how many differ at all, and the first differing byte case.
 #include <cstdint>
 
 #include "nvfp4.h"
@@ -32,40 +34,46 @@ __device__ __forceinline__ uint32_t mix32(uint32_t x) {  // a 32-bit integer has
 }
 
 // out[0] = differing bytes, out[1] = differing normal quotients,
-// out[2] = first differing byte case: (combo << 32) | (A bits << 16) | b bits,
+// out[2] = first differing byte case: (grid y << 32) | (A bits << 16) | b bits,
 // out[3] = differing quotients of any size, out[4] / out[5] = differing bytes
 // with one correction / with the bare product b * rden
 __global__ void quotient_check_kernel(unsigned long long* out) {
   const uint32_t abits = kFirstA + blockIdx.x;
-  const int combo = blockIdx.y;  // 0: Q=6 over 2688; 1: Q=6 over 1536; 2: Q=4 over 1536
-  const float A = __uint_as_float(abits << 16);
+  const int combo = blockIdx.y % 3;  // 0: Q=6 over 2688; 1: Q=6 over 1536; 2: Q=4 over 1536
+  float A = __uint_as_float(abits << 16);
+  if (blockIdx.y >= 3) {  // an fp32 amax between this bf16 value and the next
+    const uint32_t h = mix32(abits * 0x2545F491u + blockIdx.y);
+    A = __uint_as_float((abits << 16) | (h & 0xFFFFu));
+  }
   const float alpha = __fdiv_rn(A, combo == 0 ? kAlphaDen : kAlphaDen46);
   const float den = __fmul_rn(combo == 2 ? 4.0f : 6.0f, alpha);
   const float rden = (den != 0.0f) ? __frcp_rn(den) : 0.0f;
   unsigned long long bytes = 0, quots = 0, quots_all = 0, bytes1 = 0, bytes0 = 0;
-  for (uint32_t bb = threadIdx.x; bb <= abits + 256u; bb += blockDim.x) {
+  for (uint32_t bb = threadIdx.x; bb <= kLastA + 256u; bb += blockDim.x) {
     float b;
-    if (bb <= abits) {
+    if (bb <= kLastA) {
       b = __uint_as_float(bb << 16);
-    } else {  // random fp32 in [0, A]
-      const uint32_t h = mix32(abits * 0x9E3779B9u + (uint32_t)combo * 0x85EBCA6Bu + bb);
-      b = __fmul_rn(A, __fmul_rn((float)(h >> 8), 0x1p-24f));
+    } else {  // random fp32 in [0, 4A)
+      const uint32_t h = mix32(abits * 0x9E3779B9u + blockIdx.y * 0x85EBCA6Bu + bb);
+      b = __fmul_rn(A, __fmul_rn((float)(h >> 8), 0x1p-22f));
     }
     const float q = quotient_rn(b, den, rden);
     const float ref = __fdiv_rn(b, den);
-    if (__float_as_uint(q) != __float_as_uint(ref)) {
+    const uint32_t eref = e4m3_encode(ref);
+    if (__float_as_uint(q) != __float_as_uint(ref) && ref < 1.0e6f) {
       ++quots_all;
       if (ref >= 0x1p-126f) ++quots;
     }
     {  // the same with one correction, and with the bare product
       const float q0 = __fmul_rn(b, rden);
       const float q1 = __fmaf_rn(__fmaf_rn(-q0, den, b), rden, q0);
-      if (e4m3_encode(q1) != e4m3_encode(ref)) ++bytes1;
-      if (e4m3_encode(q0) != e4m3_encode(ref)) ++bytes0;
+      if (e4m3_encode(fminf(q1, 1.0e6f)) != eref) ++bytes1;
+      if (e4m3_encode(q0) != eref) ++bytes0;
     }
-    if (e4m3_encode(q) != e4m3_encode(ref)) {
+    if (scale_byte(b, den, rden) != eref) {
       ++bytes;
-      atomicCAS(out + 2, 0ull, ((unsigned long long)combo << 32) | ((unsigned long long)abits << 16) | (bb & 0xFFFFu));
+      atomicCAS(out + 2, 0ull,
+                ((unsigned long long)blockIdx.y << 32) | ((unsigned long long)abits << 16) | (bb & 0xFFFFu));
     }
   }
   if (bytes) atomicAdd(out + 0, bytes);
@@ -84,7 +92,7 @@ extern "C" {
 // out_dev: six zeroed unsigned 64-bit counters on the device (see above).
 NVFP4_API int nvfp4_test_quotient_check(unsigned long long* out_dev, void* stream) {
   if (!out_dev) return NVFP4_ERR_NULL;
-  const dim3 grid(nvfp4::kLastA - nvfp4::kFirstA + 1, 3);
+  const dim3 grid(nvfp4::kLastA - nvfp4::kFirstA + 1, 6);
   nvfp4::quotient_check_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -141,14 +141,34 @@ def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
     assert oracle.quantize(tiny, 32, am, ROW)["status"] == -7
 
 
+@pytest.mark.parametrize("scale", [1.75, 0.4])
+def test_caller_supplied_amax_single_pass(scale):
+    """Delayed scaling: nvfp4_quantize with an amax the caller supplies (here a
+    previous step's value, larger or smaller than this tensor's own) and no
+    amax pass.  A smaller amax saturates scale bytes at 448 and codes at the
+    block maximum; GPU and oracle agree bit for bit either way, for the 1D, 4/6
+    and 2D paths and with SR."""
+    bits = small_input()
+    x = to_device(bits)
+    for flags, sel in ((ROW | COL, 0), (ROW | COL | F46, 1), (ROW | COL | TWO_D, 0), (ROW | COL | SR | F46, 2)):
+        st, am = oracle.amax(bits, flags)
+        supplied = (am * np.float32(scale)).astype(np.float32)
+        g = gpu_quantize(x, flags, sel, sr_seed=9, amax=torch.from_numpy(supplied).cuda())
+        r = oracle.quantize(bits, bits.shape[1], supplied, flags, sel=sel, sr_seed=9)
+        r["amax"] = supplied
+        assert_parity(g, r, flags)
+        if scale < 1:
+            assert (g["s_row"] == 0x7E).any()  # saturated scale bytes occur
+
+
 def test_scale_quotient_equals_ieee_division_exhaustively():
     """The kernels form each scale byte from a division-free quotient (a
-    product and two residual corrections).  For every bf16 block maximum
-    b <= every accepted bf16 amax A (and 256 random fp32 maxima per A, as
-    Hadamard-transformed blocks have), at Q = 6 over 6*448 and Q = 6, 4 over
-    6*256: its E4M3 byte equals the byte of the IEEE quotient, and the
-    quotient itself is the IEEE quotient wherever that is a normal fp32
-    number (below 2^-126 the byte is 0 either way)."""
+    product and two residual corrections).  For every finite bf16 block
+    maximum b and every accepted bf16 amax A (b > A happens with a
+    caller-supplied amax), for fp32 amax values between bf16 ones, and for 256
+    random fp32 maxima per amax (Hadamard-transformed blocks), at Q = 6 over
+    6*448 and Q = 6, 4 over 6*256, its E4M3 byte equals the byte of the IEEE
+    quotient.  The bare product b * (1/den) does not have that property."""
     import ctypes
     L = nv.lib()
     f = L.nvfp4_test_quotient_check
