@@ -83,7 +83,8 @@ enum {
   NVFP4_RHT_ROW = 8,  /* [P1] 2b: 16-point RHT along rows before quantizing R            */
   NVFP4_RHT_COL = 16, /* [P1] 2b: 16-point RHT along columns before quantizing C         */
   NVFP4_SR = 32,      /* [P1] 2d: stochastic rounding (Philox4x32-10) instead of RN      */
-  NVFP4_46 = 64       /* [P2] Methodology: 4/6 adaptive block scale; alpha over 6*256    */
+  NVFP4_46 = 64,      /* [P2] Methodology: 4/6 adaptive block scale; alpha over 6*256    */
+  NVFP4_SF_SWIZZLED = 128 /* scales in the tiled layout of block-scaled MMA operands (below) */
 };
 
 typedef enum {
@@ -144,6 +145,19 @@ NVFP4_API int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, ui
  *                   untouched on success (the caller zeroes it)
  * With 2D, the tile scale is repeated in the 1x16 scale layouts (16 times in
  * s_row, 16 times in s_col) and C's codes are exactly the transpose of R's.
+ *
+ * Scale layouts.  Plain (default): s_row is M x N/16 row-major, s_col is
+ * N x M/16 row-major.  With NVFP4_SF_SWIZZLED each copy's scale matrix
+ * (R rows x C = K/16 scale columns: R = M, K = N for s_row; R = N, K = M for
+ * s_col) is stored in tiles of 128 rows x 4 scale columns, 512 bytes each,
+ * tiles in row-major order over the padded matrix (R rounded up to 128 rows,
+ * C to 4 columns), and inside a tile scale (r, c) at byte
+ * (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4 -- the order in which a
+ * block-scaled tensor-core MMA (FP4 operand with one E4M3 scale per 16 values
+ * along K) takes its scale factors, so a GEMM can read the scales directly.
+ * The buffer then holds ceil(R/128)*128 * ceil(C/4)*4 bytes; entries of the
+ * padding are not written (zero them if the consumer reads them).  Codes are
+ * unaffected.  nvfp4_dequantize reads the plain layout only.
  */
 NVFP4_API int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const float* amax_dev,
                    uint32_t flags, int sel, uint64_t sr_seed, uint64_t rht_seed,

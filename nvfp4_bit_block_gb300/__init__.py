@@ -28,7 +28,7 @@ __all__ = [
     "nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_strerror", "output_shapes",
 ]
 
-ROWWISE, COLWISE, TWO_D, RHT_ROW, RHT_COL, SR, FOUR_SIX = 1, 2, 4, 8, 16, 32, 64
+ROWWISE, COLWISE, TWO_D, RHT_ROW, RHT_COL, SR, FOUR_SIX, SF_SWIZZLED = 1, 2, 4, 8, 16, 32, 64, 128
 SEL_MAE, SEL_MSE, SEL_MAXERR = 0, 1, 2
 
 _lib: Optional[ctypes.CDLL] = None
@@ -96,12 +96,22 @@ def _matrix(x):
     return x.data_ptr(), x.size(0), x.size(1), ld
 
 
+def _scale_shape(rows: int, cols: int, swizzled: bool):
+    """rows x cols scales; in the tiled layout rows pad to 128 and cols to 4."""
+    if not swizzled:
+        return (rows, cols)
+    return (-(-rows // 128) * 128, -(-cols // 4) * 4)
+
+
 def output_shapes(M: int, N: int, flags: int):
-    """Shapes of (q_row, s_row, q_col, s_col) for an M x N tensor (None = not produced)."""
+    """Shapes of (q_row, s_row, q_col, s_col) for an M x N tensor (None = not produced).
+    With SF_SWIZZLED a scale buffer holds the padded tiled layout (its bytes
+    are not a row-major matrix)."""
     row = bool(flags & ROWWISE)
     col = bool(flags & COLWISE)
-    return ((M, N // 2) if row else None, (M, N // 16) if row else None,
-            (N, M // 2) if col else None, (N, M // 16) if col else None)
+    swz = bool(flags & SF_SWIZZLED)
+    return ((M, N // 2) if row else None, _scale_shape(M, N // 16, swz) if row else None,
+            (N, M // 2) if col else None, _scale_shape(N, M // 16, swz) if col else None)
 
 
 @dataclass
@@ -133,7 +143,10 @@ def nvfp4_quantize(x, amax, flags: int, sel: int = SEL_MAE, sr_seed: int = 0, rh
     if out is None:
         shapes = output_shapes(M, N, flags)
         mk = lambda s: None if s is None else torch.empty(s, dtype=torch.uint8, device=x.device)
-        out = Quantized(*(mk(s) for s in shapes),
+        mks = mk if not flags & SF_SWIZZLED else (  # tiled scales: padding entries zero
+            lambda s: None if s is None else torch.zeros(s, dtype=torch.uint8, device=x.device))
+        q_row, s_row, q_col, s_col = shapes
+        out = Quantized(mk(q_row), mks(s_row), mk(q_col), mks(s_col),
                         alpha=torch.empty(2, dtype=torch.float32, device=x.device),
                         status=torch.zeros(1, dtype=torch.int32, device=x.device))
     _check(lib().nvfp4_quantize(p, M, N, ld, _ptr(amax), flags, sel, sr_seed, rht_seed, counter_offset,

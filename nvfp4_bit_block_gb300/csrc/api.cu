@@ -9,8 +9,8 @@
 
 namespace {
 
-constexpr uint32_t kKnownFlags =
-    NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_2D | NVFP4_RHT_ROW | NVFP4_RHT_COL | NVFP4_SR | NVFP4_46;
+constexpr uint32_t kKnownFlags = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_2D | NVFP4_RHT_ROW | NVFP4_RHT_COL | NVFP4_SR |
+                                  NVFP4_46 | NVFP4_SF_SWIZZLED;
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
@@ -120,6 +120,7 @@ int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const fl
   a.sel = (flags & NVFP4_46) ? sel : NVFP4_SEL_MAE;
   a.rht_row = (flags & NVFP4_RHT_ROW) ? 1 : 0;
   a.rht_col = (flags & NVFP4_RHT_COL) ? 1 : 0;
+  a.sf_swz = (flags & NVFP4_SF_SWIZZLED) ? 1 : 0;
   a.test_skip_copy = g_skip_next_copy;
   g_skip_next_copy = 0;
   const bool q46 = (flags & NVFP4_46) != 0, sr = (flags & NVFP4_SR) != 0;

@@ -284,7 +284,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
     if (ROW && rr < rows) {
       uint8_t* qt = a.q_row + (R0 + rr) * hN + C0 / 2 + 8 * rq;
-      uint8_t* st = a.s_row + (R0 + rr) * sN + C0 / 16 + rq;
+      // scale of block rq + 4k: plain layout st + 4k; tiled layout st + 512k
+      uint8_t* st = a.s_row + (a.sf_swz ? tile::sf_swz_off(R0 + rr, C0 / 16 + rq, (sN + 3) / 4)
+                                        : (R0 + rr) * sN + C0 / 16 + rq);
+      const int st_step = a.sf_swz ? 512 : 4;
       const uint64_t ct = a.ctr_off + (uint64_t)((R0 + rr) * N + C0 + 16 * rq);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // block rq + 4k of row rr
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
         uint32_t e;
         quant_block16<Q46, SR, SEL>(z, scR, w, e6, e4, codes, e);
         *reinterpret_cast<uint2*>(qt + 32 * k) = codes;
-        st[4 * k] = (uint8_t)e;
+        st[st_step * k] = (uint8_t)e;
       }
     }
     if (kStash) __syncthreads();
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
       }
     }
     __syncthreads();  // tile buffer free for the next copy; staging complete
-    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
+    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid, a.sf_swz != 0);
   }
 }
 

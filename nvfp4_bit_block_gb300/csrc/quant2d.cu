@@ -241,12 +241,14 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
       }
     }
     if (ROW && valid && ch == 0) {
-      uint8_t* sr = a.s_row + grow0 * sN + gcol0 / 16;
+      // 8 consecutive rows from a multiple of 8: 16 bytes apart in the tiled layout
+      uint8_t* sr = a.s_row + (a.sf_swz ? tile::sf_swz_off(grow0, gcol0 / 16, (sN + 3) / 4) : grow0 * sN + gcol0 / 16);
+      const int64_t sr_step = a.sf_swz ? 16 : sN;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sr[i * sN] = (uint8_t)s.e;
+      for (int i = 0; i < 8; ++i) sr[i * sr_step] = (uint8_t)s.e;
     }
     __syncthreads();  // tile buffer free for the next copy; staging complete
-    if (COL) tile::write_col_outputs<true>(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid);
+    if (COL) tile::write_col_outputs<true>(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid, a.sf_swz != 0);
   }
 }
 

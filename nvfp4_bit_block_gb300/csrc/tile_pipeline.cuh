@@ -120,6 +120,13 @@ __device__ __forceinline__ void st_v8(uint8_t* p, uint2 a, uint2 b, uint2 c, uin
                : "memory");
 }
 
+// Byte offset of scale (r, c) in the tiled layout of block-scaled MMA
+// operands: 128 x 4 tiles of 512 bytes in row-major tile order (ctiles tiles
+// per tile row), (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4 inside a tile.
+__device__ __forceinline__ int64_t sf_swz_off(int64_t r, int64_t c, int64_t ctiles) {
+  return ((r >> 7) * ctiles + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
 // Padded staging (PAD = true) for writers whose lanes hold columns 8 apart:
 // 16 bytes after every 16 columns of codes and 4 bytes after every 8 columns
 // of scales spread such lanes over all banks.
@@ -131,9 +138,12 @@ __device__ __forceinline__ int sstage_off_pad(int c) { return 4 * c + 4 * (c >> 
 
 // Write the staged columnwise outputs of one tile: tile column `c` (one per
 // thread) gets its codes for up to 64 rows (32 bytes) and up to 4 scales.
+// With swz the scales go to the tiled layout (their four row blocks stay
+// four consecutive bytes there, as the tile origin is a multiple of 64 rows).
 template <bool PAD = false>
 __device__ __forceinline__ void write_col_outputs(const uint8_t* cstage, const uint8_t* sstage, uint8_t* q_col,
-                                                  uint8_t* s_col, int64_t M, int64_t N, Coord tc, int c) {
+                                                  uint8_t* s_col, int64_t M, int64_t N, Coord tc, int c,
+                                                  bool swz = false) {
   const int64_t gc = tc.C0 + c;
   if (gc >= N) return;
   int64_t nrb = (M - tc.R0) / 16;
@@ -153,7 +163,7 @@ __device__ __forceinline__ void write_col_outputs(const uint8_t* cstage, const u
     for (int rb = 0; rb < nrb; ++rb) *reinterpret_cast<uint2*>(dst + 8 * rb) = w[rb];
   }
   const uint32_t sw = *reinterpret_cast<const uint32_t*>(sstage + (PAD ? sstage_off_pad(c) : c * 4));
-  uint8_t* sdst = s_col + gc * (M / 16) + tc.R0 / 16;
+  uint8_t* sdst = s_col + (swz ? sf_swz_off(gc, tc.R0 / 16, (M / 16 + 3) / 4) : gc * (M / 16) + tc.R0 / 16);
   if (nrb == 4 && (reinterpret_cast<uintptr_t>(sdst) & 3) == 0) {
     *reinterpret_cast<uint32_t*>(sdst) = sw;
   } else {

@@ -141,6 +141,49 @@ def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
     assert oracle.quantize(tiny, 32, am, ROW)["status"] == -7
 
 
+def relayout_tiled(plain: np.ndarray) -> np.ndarray:
+    """Plain R x C scales -> the tiled layout of block-scaled MMA operands,
+    from its definition: 128-row x 4-column tiles of 512 bytes in row-major
+    tile order over the padded matrix, scale (r, c) at byte
+    (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4 of its tile; padding zero."""
+    R, C = plain.shape
+    Rp, Cp = -(-R // 128) * 128, -(-C // 4) * 4
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * (Cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4
+    out = np.zeros(Rp * Cp, np.uint8)
+    out[off] = plain
+    return out.reshape(Rp, Cp)
+
+
+def test_relayout_reference_is_a_bijection():
+    """The test's relayout places every scale of a padded matrix exactly once."""
+    plain = np.arange(256 * 8, dtype=np.int64).reshape(256, 8) % 251 + 1
+    tiled = relayout_tiled(plain.astype(np.uint8))
+    assert tiled.size == plain.size and np.count_nonzero(tiled) == plain.size
+    assert tiled.reshape(-1)[:16].tolist() == [plain[0, 0], plain[0, 1], plain[0, 2], plain[0, 3],
+                                               plain[32, 0], plain[32, 1], plain[32, 2], plain[32, 3],
+                                               plain[64, 0], plain[64, 1], plain[64, 2], plain[64, 3],
+                                               plain[96, 0], plain[96, 1], plain[96, 2], plain[96, 3]]
+
+
+@pytest.mark.parametrize("flags", [ROW | COL, ROW | COL | F46, ROW | COL | TWO_D, ROW | COL | RHT_COL | SR, ROW, COL])
+def test_swizzled_scales_are_the_plain_scales_relaid(flags):
+    """NVFP4_SF_SWIZZLED writes each copy's scales in the tiled MMA operand
+    layout (padding rows to 128 and scale columns to 4, padding untouched);
+    codes are unchanged.  Shapes include partial tiles in both directions."""
+    for M, N in ((272, 528), (400, 1040)):
+        bits = small_input(M, N)
+        x = to_device(bits)
+        g = gpu_quantize(x, flags, 1, sr_seed=5, rht_seed=6)
+        gs = gpu_quantize(x, flags | nv.SF_SWIZZLED, 1, sr_seed=5, rht_seed=6)
+        for which in ("row", "col"):
+            if g[f"q_{which}"] is None:
+                continue
+            assert np.array_equal(gs[f"q_{which}"], g[f"q_{which}"])
+            assert np.array_equal(gs[f"s_{which}"], relayout_tiled(g[f"s_{which}"]))
+
+
 @pytest.mark.parametrize("scale", [1.75, 0.4])
 def test_caller_supplied_amax_single_pass(scale):
     """Delayed scaling: nvfp4_quantize with an amax the caller supplies (here a
