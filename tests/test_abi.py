@@ -66,7 +66,7 @@ def quantize(L, x=ALIGNED, M=32, N=32, ld=32, amax=ALIGNED2, flags=3, sel=0,
 
 def test_quantize_rejects_bad_arguments(L):
     assert quantize(L, flags=0) == -4                          # no copy requested
-    assert quantize(L, flags=3 | 128) == -4                    # unknown bit
+    assert quantize(L, flags=3 | 256) == -4                    # unknown bit
     assert quantize(L, flags=3 | 4 | 8) == -4                  # 2D with an RHT flag
     assert quantize(L, flags=2 | 8) == -4                      # row RHT without the row copy
     assert quantize(L, flags=1 | 16) == -4                     # col RHT without the col copy
