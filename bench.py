@@ -12,6 +12,7 @@ The roofline entry is for the dominant kernel (quantize), timed with CUDA
 events on its own stream inside the same rotating stream of steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py --report | --error-analysis | --once
 
 Under torchrun (N > 1) every rank runs an independent replica (the path needs
 no exchange for independent tensors) and rank 0 prints the JSON line with the
@@ -429,6 +430,49 @@ def run_report(args):
         torch.cuda.empty_cache()
 
 
+def run_error_analysis(args, nbins: int = 24):
+    """Where the rounding error sits within the blocks of the workload's
+    rowwise copy: standard NVFP4 (block max at 6, alpha over 6*448) against
+    4/6 with each selection rule.  One JSON line per variant with, per bin of
+    v = 6|x|/b (b = block max), the count, the mean and the RMS of
+    e = 6|x - x^|/b, plus the means over v in [4, 6] (the 4-6 gap) and over all
+    elements, and the time of the histogram kernel."""
+    import torch
+    import nvfp4_bit_block_gb300 as nv
+    nv.build()
+    bits = synthetic.workload(args.workload)
+    M, N = bits.shape
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    lo = int(4 * nbins / 6)
+    variants = [("standard (max 6, 448)", nv.ROWWISE, 0), ("4/6 MAE", nv.ROWWISE | nv.FOUR_SIX, 0),
+                ("4/6 MSE", nv.ROWWISE | nv.FOUR_SIX, 1), ("4/6 MAXERR", nv.ROWWISE | nv.FOUR_SIX, 2)]
+    for label, flags, sel in variants:
+        amax = nv.nvfp4_amax(x, flags)
+        out = nv.nvfp4_quantize(x, amax, flags, sel)
+        h = nv.nvfp4_error_histogram(x, out.q_row, out.s_row, out.alpha[:1], nbins)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h2 = torch.zeros_like(h)
+        e0.record()
+        nv.nvfp4_error_histogram(x, out.q_row, out.s_row, out.alpha[:1], nbins, out=h2)
+        e1.record()
+        torch.cuda.synchronize()
+        hist = h.cpu().numpy().astype(np.float64)
+        cnt, se, see = hist[0], hist[1] / 2.0 ** 24, hist[2] / 2.0 ** 32
+        with np.errstate(invalid="ignore", divide="ignore"):
+            mean = np.where(cnt > 0, se / cnt, 0.0)
+            rms = np.sqrt(np.where(cnt > 0, see / cnt, 0.0))
+        bins = [[round(6 * i / nbins, 4), round(6 * (i + 1) / nbins, 4), int(cnt[i]), round(float(mean[i]), 5),
+                 round(float(rms[i]), 5)] for i in range(nbins)]
+        print(json.dumps({
+            "analysis": "error_histogram", "workload": args.workload, "M": M, "N": N, "variant": label,
+            "flags": flags, "selection": sel, "copy": "rowwise",
+            "bins [v_lo, v_hi, count, mean e, rms e]": bins,
+            "mean_e_v_4_to_6": round(float(se[lo:].sum() / max(cnt[lo:].sum(), 1)), 5),
+            "mean_e_all": round(float(se.sum() / max(cnt.sum(), 1)), 5),
+            "rms_e_all": round(float(np.sqrt(see.sum() / max(cnt.sum(), 1))), 5),
+            "histogram_kernel_ms": round(e0.elapsed_time(e1), 4)}), flush=True)
+
+
 def run_oracle_sample(args, max_seconds: float = 20.0):
     """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
     import oracle
@@ -473,7 +517,12 @@ def main():
                     help="run amax + quantize three times on the workload and exit (for profilers)")
     ap.add_argument("--report", action="store_true",
                     help="print one JSON line per workload, ablation and X-path size (2^20..2^30)")
+    ap.add_argument("--error-analysis", action="store_true",
+                    help="print the rowwise error histogram over the scaled value, standard vs 4/6")
     args = ap.parse_args()
+    if args.error_analysis:
+        run_error_analysis(args)
+        return
     if args.once:
         run_once(args)
         return

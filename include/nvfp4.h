@@ -178,6 +178,29 @@ NVFP4_API int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld
 NVFP4_API int nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, const float* alpha_dev,
                      int64_t rows, int64_t cols, int out_is_bf16, void* out_dev, void* stream);
 
+/*
+ * nvfp4_error_histogram -- where the rounding error of a rowwise copy sits
+ * within its blocks (the 4/6 page's Problem statement: values between 4 and 6
+ * at block scale 6, around scaled value 5, carry the damaging error).
+ *
+ *   x_dev      bf16 M x N (row stride ld elements), the tensor that was quantized
+ *   q_dev      its rowwise codes (M x N/2), s_dev its rowwise scales in the
+ *              plain layout (M x N/16), alpha_dev the copy's alpha (one float)
+ *   nbins      1..1024 equal bins over v = 6|x|/b in [0, 6], b = the
+ *              element's block maximum (bin = min(floor(v*nbins/6), nbins-1))
+ *   hist_dev   unsigned 64-bit [3][nbins] on the device, ADDED to (zero it
+ *              first): element counts; sums of e = 6|x - x^|/b in units of
+ *              2^-24; sums of e*e in units of 2^-32 (each term truncated);
+ *              x^ as nvfp4_dequantize reconstructs it.  Blocks with b = 0
+ *              are skipped.  Integer sums: the result is exact and
+ *              independent of the launch configuration.
+ * Asynchronous on `stream`.  Errors: SHAPE (N % 16, ld < N, nbins out of
+ * range), NULL, ALIGN (x 16-byte, q 8-byte, ld % 8), CUDA.
+ */
+NVFP4_API int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int64_t ld, const uint8_t* q_dev,
+                                    const uint8_t* s_dev, const float* alpha_dev, int nbins,
+                                    unsigned long long* hist_dev, void* stream);
+
 /* Human-readable name of a status value (static string). */
 NVFP4_API const char* nvfp4_strerror(int status);
 

@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_dequantize.restype = c.c_int
         L.nvfp4_dequantize.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int64, c.c_int,
                                        c.c_void_p, c.c_void_p]
+        L.nvfp4_error_histogram.restype = c.c_int
+        L.nvfp4_error_histogram.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p,
+                                            c.c_void_p, c.c_int, c.c_void_p, c.c_void_p]
         L.nvfp4_strerror.restype = c.c_char_p
         L.nvfp4_strerror.argtypes = [c.c_int]
         _lib = L
@@ -167,4 +170,18 @@ def nvfp4_dequantize(q, s, alpha, out_dtype=None, out=None, stream=None):
     bf16 = 1 if out.dtype == torch.bfloat16 else 0
     _check(lib().nvfp4_dequantize(_ptr(q), _ptr(s), _ptr(alpha), rows, cols, bf16, _ptr(out),
                                   _stream_handle(stream)), "nvfp4_dequantize")
+    return out
+
+
+def nvfp4_error_histogram(x, q_row, s_row, alpha, nbins: int = 24, out=None, stream=None):
+    """int64 [3, nbins] device tensor: per bin of v = 6|x|/b (b = block max)
+    the element count, the sum of e = 6|x - x^|/b (units 2^-24) and of e*e
+    (units 2^-32) for a rowwise copy (plain scale layout); `alpha` is a
+    one-element device view of that copy's alpha.  Added to `out` if given."""
+    import torch
+    p, M, N, ld = _matrix(x)
+    if out is None:
+        out = torch.zeros((3, nbins), dtype=torch.int64, device=x.device)
+    _check(lib().nvfp4_error_histogram(p, M, N, ld, _ptr(q_row), _ptr(s_row), _ptr(alpha), nbins, _ptr(out),
+                                       _stream_handle(stream)), "nvfp4_error_histogram")
     return out

@@ -16,7 +16,7 @@ LIB = os.path.join(BUILD, "libnvfp4.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "tmap.cu", "amax.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
-           "quant2d.cu", "dequant.cu", "selftest.cu"]
+           "quant2d.cu", "dequant.cu", "analysis.cu", "selftest.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

@@ -148,6 +148,30 @@ int nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, const float* al
   return launch_status(nvfp4::launch_dequant(a, static_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int64_t ld, const uint8_t* q_dev,
+                          const uint8_t* s_dev, const float* alpha_dev, int nbins, unsigned long long* hist_dev,
+                          void* stream) {
+  if (M < 0 || N < 0 || N % 16 || ld < N) return NVFP4_ERR_SHAPE;
+  if (nbins < 1 || nbins > 1024) return NVFP4_ERR_SHAPE;
+  if (!hist_dev) return NVFP4_ERR_NULL;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (!x_dev || !q_dev || !s_dev || !alpha_dev) return NVFP4_ERR_NULL;
+  if (!aligned(x_dev, 16) || ld % 8 || !aligned(q_dev, 8) || !aligned(alpha_dev, 4) || !aligned(hist_dev, 8))
+    return NVFP4_ERR_ALIGN;
+  if (g_fail_next_launch) return launch_status(cudaSuccess);
+  nvfp4::HistArgs a;
+  a.x = static_cast<const uint16_t*>(x_dev);
+  a.M = M;
+  a.N = N;
+  a.ld = ld;
+  a.q = q_dev;
+  a.s = s_dev;
+  a.alpha = alpha_dev;
+  a.nbins = nbins;
+  a.hist = hist_dev;
+  return launch_status(nvfp4::launch_error_hist(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char* nvfp4_strerror(int status) {
   switch (status) {
     case NVFP4_OK: return "ok";

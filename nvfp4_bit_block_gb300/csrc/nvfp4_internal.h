@@ -43,6 +43,16 @@ struct DequantArgs {
   void* out;
 };
 
+struct HistArgs {
+  const uint16_t* x;
+  int64_t M, N, ld;
+  const uint8_t* q;      // rowwise codes, M x N/2
+  const uint8_t* s;      // rowwise scales, M x N/16 (plain layout)
+  const float* alpha;    // the copy's alpha
+  int nbins;
+  unsigned long long* hist;  // [3][nbins], accumulated into
+};
+
 // TMA boxes of the bf16 input: 64 columns (128 bytes, the swizzle span) x 64 rows.
 constexpr int kBoxCols = 64;
 constexpr int kBoxRows = 64;
@@ -55,5 +65,6 @@ cudaError_t launch_quant1d_46_mse(const QuantArgs& a, bool row, bool col, bool s
 cudaError_t launch_quant1d_46_max(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
 cudaError_t launch_quant2d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_error_hist(const HistArgs& a, cudaStream_t s);
 
 }  // namespace nvfp4

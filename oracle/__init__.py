@@ -99,6 +99,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4ref_quantize.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p,
                                         c.c_uint32, c.c_int, c.c_uint64, c.c_uint64, c.c_uint64,
                                         c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
+        L.nvfp4ref_error_histogram.restype = c.c_int
+        L.nvfp4ref_error_histogram.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p,
+                                               c.c_float, c.c_int, c.c_void_p]
         L.nvfp4ref_dequantize.restype = c.c_int
         L.nvfp4ref_dequantize.argtypes = [c.c_void_p, c.c_void_p, c.c_float, c.c_int64, c.c_int64,
                                           c.c_int, c.c_void_p]
@@ -228,3 +231,17 @@ def dequantize(q: np.ndarray, s: np.ndarray, alpha: float, rows: int, cols: int,
     st = lib().nvfp4ref_dequantize(_ptr(qq), _ptr(ss), alpha, rows, cols, int(out_bf16), _ptr(out))
     assert st == OK, st
     return out
+
+
+def error_histogram(x_bf16: np.ndarray, N: int, q_row: np.ndarray, s_row: np.ndarray, alpha: float,
+                    nbins: int = 24) -> np.ndarray:
+    """uint64 [3, nbins]: counts, sums of e (units 2^-24), sums of e*e (units
+    2^-32) per bin of v = 6|x|/b for a rowwise copy (plain scale layout)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, ld = x.shape
+    q = np.ascontiguousarray(q_row, dtype=np.uint8)
+    s = np.ascontiguousarray(s_row, dtype=np.uint8)
+    hist = np.zeros((3, nbins), dtype=np.uint64)
+    st = lib().nvfp4ref_error_histogram(_ptr(x), M, N, ld, _ptr(q), _ptr(s), float(alpha), nbins, _ptr(hist))
+    assert st == OK, st
+    return hist

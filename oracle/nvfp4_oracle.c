@@ -494,3 +494,50 @@ int nvfp4ref_dequantize(const uint8_t* q, const uint8_t* s, float alpha, int64_t
     }
   return REF_OK;
 }
+
+/* Error histogram of a rowwise copy over the scaled value ("Four Over Six
+ * (4/6)" technical summary, Problem statement: values between 4 and 6 at
+ * block scale 6 -- around scaled value 5 -- carry the rounding error that
+ * matters).  For every element of every block with a nonzero maximum b:
+ * v = (6|x|)/b, bin = min(floor((v*nbins)/6), nbins-1); e = (6|x - x^|)/b with
+ * x^ = val(q) * (e4m3(s) * alpha) as the dequantizer forms it; the bin adds 1
+ * to hist[bin], trunc(e * 2^24) to hist[nbins + bin] and trunc(e*e * 2^32) to
+ * hist[2*nbins + bin].  Each step is one float operation, in that order. */
+int nvfp4ref_error_histogram(const uint16_t* x, int64_t M, int64_t N, int64_t ld, const uint8_t* q,
+                             const uint8_t* s, float alpha, int nbins, uint64_t* hist) {
+  if (M < 0 || N < 0 || N % 16 || ld < N || nbins < 1 || nbins > 1024) return REF_ERR_SHAPE;
+  for (int64_t r = 0; r < M; ++r)
+    for (int64_t c0 = 0; c0 < N; c0 += 16) {
+      float b = 0.0f;
+      for (int j = 0; j < 16; ++j) {
+        float a = fabsf(nvfp4ref_bf16_to_f32(x[r * ld + c0 + j]));
+        if (a > b) b = a;
+      }
+      if (!(b > 0.0f)) continue;
+      float d = nvfp4ref_e4m3_value(s[r * (N / 16) + c0 / 16]) * alpha;
+      for (int j = 0; j < 16; ++j) {
+        int64_t c = c0 + j;
+        float xv = nvfp4ref_bf16_to_f32(x[r * ld + c]);
+        uint8_t byte = q[r * (N / 2) + c / 2];
+        uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+        float val = kGrid[code & 7];
+        if (code & 8) val = -val;
+        float xh = val * d;
+        float six_x = 6.0f * fabsf(xv);
+        float v = six_x / b;
+        float scaled = v * (float)nbins;
+        int bin = (int)floorf(scaled / 6.0f);
+        if (bin > nbins - 1) bin = nbins - 1;
+        float diff = xv - xh;
+        float six_e = 6.0f * fabsf(diff);
+        float e = six_e / b;
+        float e24 = e * 0x1p24f;
+        float ee = e * e;
+        float ee32 = ee * 0x1p32f;
+        hist[bin] += 1u;
+        hist[nbins + bin] += (uint64_t)e24;
+        hist[2 * nbins + bin] += (uint64_t)ee32;
+      }
+    }
+  return REF_OK;
+}

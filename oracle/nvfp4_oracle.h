@@ -98,6 +98,10 @@ int nvfp4ref_quantize(const uint16_t* x, int64_t M, int64_t N, int64_t ld, const
 int nvfp4ref_dequantize(const uint8_t* q, const uint8_t* s, float alpha, int64_t rows,
                         int64_t cols, int out_is_bf16, void* out);
 
+/* Error histogram of a rowwise copy over v = 6|x|/b (see the definition). */
+int nvfp4ref_error_histogram(const uint16_t* x, int64_t M, int64_t N, int64_t ld, const uint8_t* q,
+                             const uint8_t* s, float alpha, int nbins, uint64_t* hist);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,8 +30,9 @@ def declared_functions():
     return sorted(set(re.findall(r"^\s*NVFP4_API\s+(?:int|const char\*)\s+(nvfp4_\w+)\s*\(", text, flags=re.M)))
 
 
-def test_header_declares_the_four_entry_points():
-    assert declared_functions() == ["nvfp4_amax", "nvfp4_dequantize", "nvfp4_quantize", "nvfp4_strerror"]
+def test_header_declares_the_entry_points():
+    assert declared_functions() == ["nvfp4_amax", "nvfp4_dequantize", "nvfp4_error_histogram", "nvfp4_quantize",
+                                    "nvfp4_strerror"]
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -118,6 +119,22 @@ def test_binding_raises_without_the_library(monkeypatch, tmp_path):
         nv.lib()
 
 
+def test_error_histogram_rejects_bad_arguments(L):
+    h = L.nvfp4_error_histogram
+    h.restype = ctypes.c_int
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    ok = dict(x=ALIGNED, M=32, N=32, ld=32, q=ALIGNED, s=ALIGNED, a=ALIGNED2, nb=24, hist=ALIGNED3)
+
+    def call(**kw):
+        d = dict(ok, **kw)
+        return h(d["x"], d["M"], d["N"], d["ld"], d["q"], d["s"], d["a"], d["nb"], d["hist"], None)
+    assert call(N=40) == -2 and call(ld=16) == -2 and call(nb=0) == -2 and call(nb=1025) == -2
+    assert call(hist=None) == -1 and call(q=None) == -1
+    assert call(x=ALIGNED + 8) == -3 and call(ld=36) == -3
+    assert call(M=0) == 0
+
+
 def test_binding_has_the_c_names():
-    for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_strerror"):
+    for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_error_histogram", "nvfp4_strerror"):
         assert callable(getattr(nv, name))

@@ -156,6 +156,22 @@ def relayout_tiled(plain: np.ndarray) -> np.ndarray:
     return out.reshape(Rp, Cp)
 
 
+@pytest.mark.parametrize("flags,sel", [(ROW, 0), (ROW | F46, 0), (ROW | F46, 1), (ROW | SR, 0)])
+def test_error_histogram_matches_oracle(flags, sel):
+    """nvfp4_error_histogram (integer bins) equals the oracle's histogram of the
+    same quantized copy, on the small input and on the activation workload."""
+    for bits in (small_input(), synthetic.workload("act_46mae_8192x5120") if flags == ROW | F46 else None):
+        if bits is None:
+            continue
+        x = to_device(bits)
+        g = gpu_quantize(x, flags, sel, sr_seed=4)
+        out = g["_out"]
+        h = nv.nvfp4_error_histogram(x, out.q_row, out.s_row, out.alpha[:1], 24).cpu().numpy().astype(np.uint64)
+        r = oracle.error_histogram(bits, bits.shape[1], g["q_row"], g["s_row"], float(g["alpha"][0]), 24)
+        assert np.array_equal(h, r)
+        assert int(h[0].sum()) > 0
+
+
 def test_relayout_reference_is_a_bijection():
     """The test's relayout places every scale of a padded matrix exactly once."""
     plain = np.arange(256 * 8, dtype=np.int64).reshape(256, 8) % 251 + 1
