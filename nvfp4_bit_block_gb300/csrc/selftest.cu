@@ -1,7 +1,7 @@
 // selftest.cu -- exhaustive device check of the scale-byte quotient.
 //
 // The quantize kernels take E4M3(fl(b / den)) from scale_byte (quotient_rn:
-// a product and two residual corrections, capped at 1e6) instead of an IEEE
+// a product and one residual correction, capped at 1e6) instead of an IEEE
 // division.  This kernel compares the two bytes for every pair of a bf16
 // block maximum b (any finite value: an amax supplied by the caller may be
 // smaller than the block) and a bf16 tensor amax A that the library accepts
@@ -36,7 +36,7 @@ __device__ __forceinline__ uint32_t mix32(uint32_t x) {  // a 32-bit integer has
 // out[0] = differing bytes, out[1] = differing normal quotients,
 // out[2] = first differing byte case: (grid y << 32) | (A bits << 16) | b bits,
 // out[3] = differing quotients of any size, out[4] / out[5] = differing bytes
-// with one correction / with the bare product b * rden
+// with a second correction / with the bare product b * rden
 __global__ void quotient_check_kernel(unsigned long long* out) {
   const uint32_t abits = kFirstA + blockIdx.x;
   const int combo = blockIdx.y % 3;  // 0: Q=6 over 2688; 1: Q=6 over 1536; 2: Q=4 over 1536
@@ -64,11 +64,11 @@ __global__ void quotient_check_kernel(unsigned long long* out) {
       ++quots_all;
       if (ref >= 0x1p-126f) ++quots;
     }
-    {  // the same with one correction, and with the bare product
-      const float q0 = __fmul_rn(b, rden);
-      const float q1 = __fmaf_rn(__fmaf_rn(-q0, den, b), rden, q0);
-      if (e4m3_encode(fminf(q1, 1.0e6f)) != eref) ++bytes1;
-      if (e4m3_encode(q0) != eref) ++bytes0;
+    {  // a second correction, and the bare product, for comparison
+      const float r2 = __fmaf_rn(-q, den, b);
+      const float q2 = __fmaf_rn(r2, rden, q);
+      if (e4m3_encode(fminf(q2, 1.0e6f)) != eref) ++bytes1;
+      if (e4m3_encode(__fmul_rn(b, rden)) != eref) ++bytes0;
     }
     if (scale_byte(b, den, rden) != eref) {
       ++bytes;

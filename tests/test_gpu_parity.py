@@ -222,7 +222,7 @@ def test_caller_supplied_amax_single_pass(scale):
 
 def test_scale_quotient_equals_ieee_division_exhaustively():
     """The kernels form each scale byte from a division-free quotient (a
-    product and two residual corrections).  For every finite bf16 block
+    product and one residual correction).  For every finite bf16 block
     maximum b and every accepted bf16 amax A (b > A happens with a
     caller-supplied amax), for fp32 amax values between bf16 ones, and for 256
     random fp32 maxima per amax (Hadamard-transformed blocks), at Q = 6 over
@@ -236,7 +236,7 @@ def test_scale_quotient_equals_ieee_division_exhaustively():
     out = torch.zeros(6, dtype=torch.int64, device="cuda")
     assert f(out.data_ptr(), None) == 0
     torch.cuda.synchronize()
-    bytes_differ, _normal_quotients_differ, first, _quotients_differ, _one_step, bare = out.tolist()
+    bytes_differ, _normal_quotients_differ, first, _quotients_differ, _two_steps, bare = out.tolist()
     assert bytes_differ == 0, hex(first)
     assert bare > 0  # the bare product b * (1/den) alone is not enough
 
