@@ -62,7 +62,7 @@ typedef enum {
   NVFP4_OK = 0,
   NVFP4_ERR_NULL = -1,      /* a required pointer is NULL                            */
   NVFP4_ERR_SHAPE = -2,     /* N % 16 != 0; M % 16 != 0 with COLWISE or 2D; ld < N;
-                               negative sizes                                         */
+                               negative sizes; M or N above 2^31 - 1                  */
   NVFP4_ERR_ALIGN = -3,     /* x not 16-byte aligned or ld % 8 != 0; an output not
                                aligned to its access width                             */
   NVFP4_ERR_FLAGS = -4,     /* unknown bits; no copy requested; 2D with an RHT flag;

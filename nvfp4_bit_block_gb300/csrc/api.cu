@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 #include "nvfp4_internal.h"
 
 namespace {
@@ -29,8 +31,8 @@ int check_shape(int64_t M, int64_t N, int64_t ld, uint32_t flags) {
   if ((flags & (NVFP4_COLWISE | NVFP4_2D)) && (M % 16)) return NVFP4_ERR_SHAPE;
   if (ld < N) return NVFP4_ERR_SHAPE;
   if (ld % 8) return NVFP4_ERR_ALIGN;
-  // grid limit: row tiles (64 rows for the 1D kernels) go into gridDim.y
-  if ((M + 63) / 64 > 65535) return NVFP4_ERR_SHAPE;
+  // tile coordinates of the TMA copies are 32-bit
+  if (M > INT32_MAX || N > INT32_MAX) return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
 }
 
@@ -176,7 +178,7 @@ const char* nvfp4_strerror(int status) {
   switch (status) {
     case NVFP4_OK: return "ok";
     case NVFP4_ERR_NULL: return "a required pointer is NULL";
-    case NVFP4_ERR_SHAPE: return "bad shape (N % 16, M % 16 with COLWISE/2D, ld < N, or too many rows)";
+    case NVFP4_ERR_SHAPE: return "bad shape (N % 16, M % 16 with COLWISE/2D, ld < N, or M, N beyond 2^31 - 1)";
     case NVFP4_ERR_ALIGN: return "misaligned pointer or leading dimension";
     case NVFP4_ERR_FLAGS: return "invalid flag combination or selection rule";
     case NVFP4_ERR_CUDA: return "CUDA launch failed";

@@ -85,7 +85,7 @@ def test_quantize_rejects_bad_arguments(L):
     assert quantize(L, x=None) == -1
     assert quantize(L, q_col=None) == -1
     assert quantize(L, flags=1, q_col=None, s_col=None) != -1  # not needed without COLWISE
-    assert quantize(L, M=65535 * 64 + 16, flags=1) == -2       # beyond the row-tile grid limit
+    assert quantize(L, M=2 ** 31, N=32, flags=1) == -2         # beyond 32-bit tile coordinates
 
 
 def test_amax_and_dequantize_reject_bad_arguments(L):
