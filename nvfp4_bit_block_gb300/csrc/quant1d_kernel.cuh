@@ -12,11 +12,15 @@
 //     that each column of the transposed copy is written as one 32-byte store,
 // so every block's scale, rounding and 4/6 choice happen in one thread's
 // registers.  Element arithmetic uses packed f32x2 operations, which halve
-// the issue slots of the multiplies and fused multiply-adds.
+// the issue slots of the multiplies and fused multiply-adds.  The per-block
+// code is straight-line: scale bytes come from a division-free quotient (see
+// quotient_rn), the RHT flags and the 4/6 rule are template parameters.
 //
 // With stochastic rounding on both copies, one Philox4x32-10 call per element
 // serves both: the rowwise pass uses word 0 and parks word 1 in shared memory
-// for the columnwise pass.
+// for the columnwise pass (that 64 KB stash leaves room for one tile buffer,
+// so those kernels load each tile after the previous one is done and rely on
+// their second CTA per SM for overlap).
 //
 // Sources: "Four Over Six (4/6)" technical summary (Problem statement,
 // Methodology, Implementation details) and "Pretraining Large Language Models
