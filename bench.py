@@ -75,7 +75,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -88,7 +88,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -97,16 +97,17 @@ class ClockSampler:
     def __exit__(self, *exc):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             out, _ = self.proc.communicate(timeout=5)
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
         return False
 
-    def summary(self):
+    def summary(self, skip_first: bool = True):
+        """Median SM clock and the throttle reasons seen; the first reading
+        (taken as the sampler starts, before the load) is left out."""
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[1 if skip_first else 0:]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -180,8 +181,21 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    # the timed steps last milliseconds, shorter than the sampling interval, so
+    # the sampler also covers an untimed half second of the same steps run
+    # right before them: the clocks reported are the clocks under this load
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(max(1, 2 * nsets)):
+            graphs[k % nsets].replay()
+    torch.cuda.synchronize()
+    per_step_s = max((time.perf_counter() - t0) / max(1, 2 * nsets), 1e-6)
+    load_steps = int(min(20000, max(1, 0.5 / per_step_s)))
     with ClockSampler(dev.index) as clocks:
+        time.sleep(0.06)  # the sampler's first reading precedes the load
         with torch.cuda.stream(stream):
+            for k in range(load_steps):
+                graphs[k % nsets].replay()
             ev0.record(stream)
             for k in range(args.steps):
                 graphs[k % nsets].replay()
