@@ -122,16 +122,13 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
         for (int i = 0; i < 16; ++i) wd[i] = tile::read_pair_word(buf, 16 * rb + i, cp_p);
 #pragma unroll
         for (int i = 0; i < 16; i += 2) m_plain = absmax_nan_bf16x2(m_plain, absmax_nan_bf16x2(wd[i], wd[i + 1]));
-        if (RHT_COL) {
+        if (RHT_COL) {  // both columns at once; the 1/4 is applied to the maximum
+          float2 zp[16];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float z[16];
+          for (int i = 0; i < 16; ++i) zp[i] = bf16x2_to_f32x2(wd[i] ^ rht_mask_col(signs, i));
+          wht16_x2(zp);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = h ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
-            rht16(z, signs);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m_col = max(m_col, abs_bits(z[i]));
-          }
+          for (int i = 0; i < 16; ++i) m_col = max(m_col, max(abs_bits(zp[i].x), abs_bits(zp[i].y)));
         }
       }
     }
@@ -149,10 +146,11 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
         float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          z[2 * j] = bf16_lo(wd[j]);
-          z[2 * j + 1] = bf16_hi(wd[j]);
+          const float2 f = bf16x2_to_f32x2(wd[j] ^ rht_mask_row(signs, j));
+          z[2 * j] = f.x;
+          z[2 * j + 1] = f.y;
         }
-        rht16(z, signs);
+        wht16(z);
 #pragma unroll
         for (int j = 0; j < 16; ++j) m_row = max(m_row, abs_bits(z[j]));
       }
@@ -160,7 +158,11 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
     __syncthreads();  // the buffer is refilled by the next iteration's prefetch
   }
   const uint32_t plain = packed_to_bits(m_plain);
-  cta_reduce_and_publish(RHT_ROW ? m_row : plain, RHT_COL ? m_col : plain, a.amax);
+  // max |y| = max |t| / 4 for the unnormalised butterfly output t: the scaling
+  // is exact and rounding is monotonic, so it commutes with the maximum
+  const uint32_t quarter_row = __float_as_uint(__fmul_rn(__uint_as_float(m_row), 0.25f));
+  const uint32_t quarter_col = __float_as_uint(__fmul_rn(__uint_as_float(m_col), 0.25f));
+  cta_reduce_and_publish(RHT_ROW ? quarter_row : plain, RHT_COL ? quarter_col : plain, a.amax);
 }
 
 template <bool RHT_ROW, bool RHT_COL>

@@ -81,6 +81,15 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " sub.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // max(|a|, |b|) per bf16 half (the sign of the result is meaningless; mask it)
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -328,51 +337,58 @@ __device__ __forceinline__ float score8(const float* z, uint32_t codes, float d,
 }
 
 // ---------------------------------------------------------------- Hadamard
-// In-register 16-point random Hadamard transform: y = (1/4) H16 (s . z) with
-// H16 in Sylvester order (the iterative butterfly yields natural order).
-__device__ __forceinline__ void rht16(float* z, uint32_t signs) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if ((signs >> j) & 1u) z[j] = -z[j];
+// 16-point random Hadamard transform y = (1/4) H16 (s . z), H16 in Sylvester
+// order (the iterative butterfly yields natural order), s_j = -1 where bit j
+// of `signs` is set.  The sign flips are exact, so they are applied to the
+// packed bf16 words before widening: an XOR with a mask built from the sign
+// bits (uniform across the kernel, so the masks live in uniform registers).
+// A columnwise word holds row j of two neighbouring columns, a rowwise word
+// elements 2j and 2j+1 of one vector.
+__device__ __forceinline__ uint32_t rht_mask_col(uint32_t signs, int j) { return ((signs >> j) & 1u) * 0x80008000u; }
+__device__ __forceinline__ uint32_t rht_mask_row(uint32_t signs, int j) {
+  return (((signs >> (2 * j)) & 1u) << 15) | (((signs >> (2 * j + 1)) & 1u) << 31);
+}
+
+// Unnormalised butterfly on two vectors at once, held as pairs z[i] =
+// (element i of the first vector, element i of the second): four stages of
+// packed adds and subtracts, each rounded as its scalar counterpart.
+__device__ __forceinline__ void wht16_x2(float2* z) {
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if ((i & h) == 0) {
-        const float a = z[i], b = z[i + h];
-        z[i] = __fadd_rn(a, b);
-        z[i + h] = __fsub_rn(a, b);
+        const float2 a = z[i], b = z[i + h];
+        z[i] = add2(a, b);
+        z[i + h] = sub2(a, b);
       }
     }
   }
-#pragma unroll
-  for (int j = 0; j < 16; ++j) z[j] = __fmul_rn(z[j], 0.25f);
 }
 
-// The same transform on a 16-vector split over a lane pair: the even lane
-// holds elements 0..7, the odd lane 8..15.  All 32 lanes must call it.
-__device__ __forceinline__ void rht16_pair(float* z, uint32_t signs, bool odd) {
-  const uint32_t s = odd ? (signs >> 8) : signs;
+// Unnormalised butterfly on one vector z[0..15]: the first stage pairs
+// neighbours (scalar), the later stages pair (i, i+1) with (i+h, i+h+1)
+// (packed).  Same operations in the same order as the plain butterfly.
+__device__ __forceinline__ void wht16(float* z) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if ((s >> j) & 1u) z[j] = -z[j];
-#pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if ((i & h) == 0) {
-        const float a = z[i], b = z[i + h];
-        z[i] = __fadd_rn(a, b);
-        z[i + h] = __fsub_rn(a, b);
-      }
-    }
+  for (int i = 0; i < 16; i += 2) {
+    const float a = z[i], b = z[i + 1];
+    z[i] = __fadd_rn(a, b);
+    z[i + 1] = __fsub_rn(a, b);
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float other = __shfl_xor_sync(0xFFFFFFFFu, z[j], 1);
-    // even lane: u[j] + u[j+8]; odd lane: u[j] - u[j+8] with u[j] the partner's
-    const float r = odd ? __fsub_rn(other, z[j]) : __fadd_rn(z[j], other);
-    z[j] = __fmul_rn(r, 0.25f);
+  for (int h = 2; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      if ((i & h) == 0) {
+        const float2 a = make_float2(z[i], z[i + 1]), b = make_float2(z[i + h], z[i + h + 1]);
+        const float2 s = add2(a, b), d = sub2(a, b);
+        z[i] = s.x;
+        z[i + 1] = s.y;
+        z[i + h] = d.x;
+        z[i + h + 1] = d.y;
+      }
+    }
   }
 }
 

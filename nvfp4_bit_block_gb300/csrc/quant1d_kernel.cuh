@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
           wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
           wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
         }
+        if (kRhtRow) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wd[j] ^= rht_mask_row(signs, j);  // s . z
+        }
         float z[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -312,10 +316,15 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
         }
         float bmax;
         if (kRhtRow) {
-          rht16(z, signs);
+          wht16(z);
           bmax = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(z[j]));
+          for (int j = 0; j < 16; j += 2) {
+            const float2 y = mul2(make_float2(z[j], z[j + 1]), make_float2(0.25f, 0.25f));
+            z[j] = y.x;
+            z[j + 1] = y.y;
+            bmax = fmaxf(bmax, fmaxf(fabsf(y.x), fabsf(y.y)));
+          }
         } else {
           bmax = block_absmax16(wd);
         }
@@ -371,21 +380,27 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
                0x7FFF7FFFu;
         }
         float zz[2][16];
+        float bm[2] = {bf16_lo(m2), bf16_hi(m2)};
+        if (kRhtCol) {  // both columns' 16-vectors at once, as pairs
+          float2 zp[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 f = bf16x2_to_f32x2(wd[i]);
-          zz[0][i] = f.x;
-          zz[1][i] = f.y;
-        }
-        float bm[2];
+          for (int i = 0; i < 16; ++i) zp[i] = bf16x2_to_f32x2(wd[i] ^ rht_mask_col(signs, i));
+          wht16_x2(zp);
+          bm[0] = bm[1] = 0.0f;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          bm[h] = h ? bf16_hi(m2) : bf16_lo(m2);
-          if (kRhtCol) {
-            rht16(zz[h], signs);
-            bm[h] = 0.0f;
+          for (int i = 0; i < 16; ++i) {
+            const float2 y = mul2(zp[i], make_float2(0.25f, 0.25f));
+            zz[0][i] = y.x;
+            zz[1][i] = y.y;
+            bm[0] = fmaxf(bm[0], fabsf(y.x));
+            bm[1] = fmaxf(bm[1], fabsf(y.y));
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) bm[h] = fmaxf(bm[h], fabsf(zz[h][i]));
+          for (int i = 0; i < 16; ++i) {
+            const float2 f = bf16x2_to_f32x2(wd[i]);
+            zz[0][i] = f.x;
+            zz[1][i] = f.y;
           }
         }
         uint32_t e6[2], e4[2];
