@@ -13,6 +13,9 @@
 // (Hadamard) block has.  It reports how many scale bytes differ, how many
 // quotients differ where the IEEE quotient is a normal fp32 number below the
 // cap, how many differ at all, and the first differing byte case.
+//
+// A second hook runs the kernels' Hadamard transform alone, so that the
+// transformed values themselves can be compared with a reference.
 #include <cstdint>
 
 #include "nvfp4.h"
@@ -94,6 +97,74 @@ NVFP4_API int nvfp4_test_quotient_check(unsigned long long* out_dev, void* strea
   if (!out_dev) return NVFP4_ERR_NULL;
   const dim3 grid(nvfp4::kLastA - nvfp4::kFirstA + 1, 6);
   nvfp4::quotient_check_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(out_dev);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// The kernels' 16-point random Hadamard transform, alone: out (fp32, M x N)
+// holds y = (1/4) H16 (s . x) of every 16-vector along rows (along_cols = 0)
+// or along columns (along_cols = 1), formed with the same masks and packed
+// butterflies as the quantize kernels (one thread per vector pair).
+__global__ void rht_check_kernel(const uint16_t* x, int64_t M, int64_t N, int64_t ld, int along_cols,
+                                 uint32_t k0, uint32_t k1, float* out) {
+  const uint32_t signs = rht_sign_bits(k0, k1);
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (!along_cols) {  // one rowwise vector per thread
+    const int64_t nv = M * (N / 16);
+    if (t >= nv) return;
+    const int64_t r = t / (N / 16), c0 = (t - r * (N / 16)) * 16;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(x + r * ld + c0);
+    float z[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = bf16x2_to_f32x2(w[j] ^ rht_mask_row(signs, j));
+      z[2 * j] = f.x;
+      z[2 * j + 1] = f.y;
+    }
+    wht16(z);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[r * N + c0 + j] = __fmul_rn(z[j], 0.25f);
+  } else {  // two columnwise vectors (columns 2p, 2p+1, rows 16b..16b+15) per thread
+    const int64_t nv = (M / 16) * (N / 2);
+    if (t >= nv) return;
+    const int64_t b = t / (N / 2), p = t - b * (N / 2);
+    float2 zp[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(x + (16 * b + i) * ld + 2 * p);
+      zp[i] = bf16x2_to_f32x2(w ^ rht_mask_col(signs, i));
+    }
+    wht16_x2(zp);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 y = mul2(zp[i], make_float2(0.25f, 0.25f));
+      out[(16 * b + i) * N + 2 * p] = y.x;
+      out[(16 * b + i) * N + 2 * p + 1] = y.y;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+// Test hook (not declared in nvfp4.h): the kernels' Hadamard transform of a
+// bf16 M x N tensor (row stride ld, 4-byte aligned rows), 16-vectors along
+// rows or columns, into a dense fp32 M x N buffer.
+NVFP4_API int nvfp4_test_rht(const void* x_dev, int64_t M, int64_t N, int64_t ld, int along_cols, uint64_t rht_seed,
+                             float* out_dev, void* stream) {
+  if (!x_dev || !out_dev) return NVFP4_ERR_NULL;
+  if (M <= 0 || N <= 0 || N % 16 || ld < N || ld % 2 || (along_cols && M % 16)) return NVFP4_ERR_SHAPE;
+  const int64_t nv = along_cols ? (M / 16) * (N / 2) : M * (N / 16);
+  const int64_t grid = (nv + 255) / 256;
+  nvfp4::rht_check_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(x_dev), M, N, ld, along_cols, (uint32_t)rht_seed, (uint32_t)(rht_seed >> 32),
+      out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

@@ -220,6 +220,42 @@ def test_caller_supplied_amax_single_pass(scale):
             assert (g["s_row"] == 0x7E).any()  # saturated scale bytes occur
 
 
+@pytest.mark.parametrize("along_cols", [0, 1])
+def test_transformed_values_agree_with_the_oracle(along_cols):
+    """The tolerance on transformed values: the kernels' fp32 Hadamard
+    transform (run alone through a test hook, same device code) agrees with
+    the oracle's (double precision, rounded once) within 1e-6 of each
+    16-vector's 2-norm, for vectors along rows and along columns."""
+    import ctypes
+    L = nv.lib()
+    f = L.nvfp4_test_rht
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    M, N, seed = 272, 528, 0xC0FFEE
+    bits = small_input(M, N, kind="grad")
+    x = to_device(bits)
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    assert f(x.data_ptr(), M, N, N, along_cols, seed, out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    g = out.cpu().numpy()
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)
+    signs = oracle.rht_signs(seed)
+    worst = 0.0
+    if along_cols:
+        vecs = [(slice(16 * b, 16 * b + 16), c) for b in range(M // 16) for c in range(N)]
+    else:
+        vecs = [(r, slice(16 * k, 16 * k + 16)) for r in range(M) for k in range(N // 16)]
+    for idx in vecs:
+        v = xf[idx]
+        ref = oracle.rht16(v, signs)
+        norm = float(np.linalg.norm(v.astype(np.float64)))
+        err = float(np.abs(g[idx].astype(np.float64) - ref.astype(np.float64)).max())
+        assert err <= 1e-6 * norm, (idx, err, norm)
+        worst = max(worst, err / norm if norm else 0.0)
+    assert worst < 1e-6
+
+
 def test_scale_quotient_equals_ieee_division_exhaustively():
     """The kernels form each scale byte from a division-free quotient (a
     product and one residual correction).  For every finite bf16 block
