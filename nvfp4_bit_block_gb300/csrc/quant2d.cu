@@ -58,27 +58,47 @@ __device__ __forceinline__ void patch_row(const uint8_t* pbase, int c, int i, fl
   }
 }
 
-// 4/6 score of the 16x16 block at scale s: per row a tree over this lane's 8
-// columns plus the column partner's, then a tree over this row half's 8 rows,
-// then the two row halves.  Same order as a perfect binary tree over the 256
-// elements in row-major order.
-template <bool SR>
-__device__ __forceinline__ float block_score(const uint8_t* pbase, int c, const BlockScale& s, float Q,
-                                             const QuantArgs& a, int64_t grow0, int64_t gcol0, int sel) {
-  float rows[8];
+// One 4/6 candidate on one patch row: the 8 codes at scale s (maximum Q) and
+// this row part's score -- err = z - val*d rounded once, |err| (MAE, MAXERR)
+// or err*err (MSE), combined as the perfect binary tree over the 8 values in
+// order.  The row's two column halves, the 8 rows of a half and the two halves
+// are combined by the caller, so the score of the 16x16 block is the same
+// tree over its 256 values in row-major order.
+template <bool SR, int SEL>
+__device__ __forceinline__ float cand8(const float* z, const BlockScale& s, float Q, const uint32_t* w,
+                                       uint32_t& codes) {
+  const float2 inv2 = make_float2(s.inv, s.inv);
+  const float2 nd = make_float2(-s.d, -s.d);
+  float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float z[8], v[8];
-    patch_row(pbase, c, i, z);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = scaled<SR>(z[j], s, Q, SR ? word0_of(a, grow0 + i, gcol0 + j) : 0u);
-    const float part = score8(z, e2m1x8(v), s.d, sel);
-    rows[i] = err_combine(part, __shfl_xor_sync(0xFFFFFFFFu, part, 1), sel);
+  for (int j = 0; j < 4; ++j) {
+    const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
+    v[2 * j] = r.x;
+    v[2 * j + 1] = r.y;
   }
-  const float h = err_combine(err_combine(err_combine(rows[0], rows[1], sel), err_combine(rows[2], rows[3], sel), sel),
-                              err_combine(err_combine(rows[4], rows[5], sel), err_combine(rows[6], rows[7], sel), sel),
-                              sel);
-  return err_combine(h, __shfl_xor_sync(0xFFFFFFFFu, h, 16), sel);
+  if (SR) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = sr_round(v[j], Q, w[j]);
+  } else if (Q == 4.0f && max4_needs_clamp(s.e)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
+  }
+  uint32_t h[4];
+  codes = e2m1x8_enc_dec(v, h);
+  float t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 err = fma2(f16x2_to_f32x2(h[k]), nd, make_float2(z[2 * k], z[2 * k + 1]));
+    if (SEL == kSelMSE) {
+      const float2 sq = mul2(err, err);
+      t[k] = __fadd_rn(sq.x, sq.y);
+    } else if (SEL == kSelMax) {
+      t[k] = fmaxf(fabsf(err.x), fabsf(err.y));
+    } else {
+      t[k] = __fadd_rn(fabsf(err.x), fabsf(err.y));
+    }
+  }
+  return err_combine(err_combine(t[0], t[1], SEL), err_combine(t[2], t[3], SEL), SEL);
 }
 
 // Byte m of each of w[0..3] gathered into output word m (a 4 x 4 byte transpose).
@@ -91,7 +111,7 @@ __device__ __forceinline__ void transpose4x4(const uint32_t* w, uint32_t* t) {
   t[3] = __byte_perm(a_hi, b_hi, 0x7632);
 }
 
-template <bool ROW, bool COL, bool Q46, bool SR>
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
 __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) ? 2 : 3))
     quant2d_kernel(const QuantArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -175,53 +195,81 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 1));
     bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, 16));
 
-    BlockScale s = block_scale(bmax, alpha, 6.0f);
-    float Q = 6.0f;
-    if (Q46) {
-      const BlockScale s4 = block_scale(bmax, alpha, 4.0f);
-      const float sc6 = block_score<SR>(pbase, pc, s, 6.0f, a, grow0, gcol0, a.sel);
-      const float sc4 = block_score<SR>(pbase, pc, s4, 4.0f, a, grow0, gcol0, a.sel);
-      if (sc4 < sc6) {
-        s = s4;
-        Q = 4.0f;
-      }
-    }
-    const bool clamp = !SR && Q == 4.0f && max4_needs_clamp(s.e);  // RN at a subnormal or saturated max-4 scale
-
-    // a7 + a9: each element encoded once; rows of codes go to R directly,
-    // and pairs of rows become C bytes
+    // a9: a patch row's code word goes to R directly, and each pair of rows
+    // becomes C bytes (column j = 2m: byte m of lo; j = 2m+1: byte m of hi;
+    // the first row in the low nibble)
     uint32_t lo[4], hi[4];
     uint8_t* qr = a.q_row + grow0 * hN + gcol0 / 2;
+    auto store_row = [&](int i, uint32_t c) {
+      if (ROW && valid) *reinterpret_cast<uint32_t*>(qr + i * hN) = c;
+    };
+    auto interleave = [&](int p2, uint32_t c0, uint32_t c1) {
+      lo[p2] = (c0 & 0x0F0F0F0Fu) | ((c1 & 0x0F0F0F0Fu) << 4);
+      hi[p2] = ((c0 >> 4) & 0x0F0F0F0Fu) | (c1 & 0xF0F0F0F0u);
+    };
+
+    // a6-a8: each element is scaled and rounded once per candidate
+    BlockScale s = block_scale(bmax, alpha, 6.0f);
+    if (Q46) {  // both candidates scored in one pass; both candidates' code rows kept
+      const BlockScale s4 = block_scale(bmax, alpha, 4.0f);
+      uint32_t code6[8], code4[8];
+      float r6[8], r4[8];
 #pragma unroll
-    for (int p2 = 0; p2 < 4; ++p2) {
-      uint32_t code[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = 2 * p2 + h;
-        float z[8], v[8];
+      for (int i = 0; i < 8; ++i) {
+        float z[8];
         patch_row(pbase, pc, i, z);
+        uint32_t w[8];
         if (SR) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = scaled<true>(z[j], s, Q, word0_of(a, grow0 + i, gcol0 + j));
-        } else {
-          const float2 inv2 = make_float2(s.inv, s.inv);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
-            v[2 * j] = r.x;
-            v[2 * j + 1] = r.y;
-          }
-          if (clamp) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = fminf(fmaxf(v[j], -4.0f), 4.0f);
-          }
+          for (int j = 0; j < 8; ++j) w[j] = word0_of(a, grow0 + i, gcol0 + j);
         }
-        code[h] = e2m1x8(v);
-        if (ROW && valid) *reinterpret_cast<uint32_t*>(qr + i * hN) = code[h];
+        const float p6 = cand8<SR, SEL>(z, s, 6.0f, w, code6[i]);
+        const float p4 = cand8<SR, SEL>(z, s4, 4.0f, w, code4[i]);
+        r6[i] = err_combine(p6, __shfl_xor_sync(0xFFFFFFFFu, p6, 1), SEL);
+        r4[i] = err_combine(p4, __shfl_xor_sync(0xFFFFFFFFu, p4, 1), SEL);
       }
-      // column j = 2m: byte m of lo; j = 2m+1: byte m of hi (row i low nibble)
-      lo[p2] = (code[0] & 0x0F0F0F0Fu) | ((code[1] & 0x0F0F0F0Fu) << 4);
-      hi[p2] = ((code[0] >> 4) & 0x0F0F0F0Fu) | (code[1] & 0xF0F0F0F0u);
+      auto tree8 = [](const float* r) {
+        return err_combine(err_combine(err_combine(r[0], r[1], SEL), err_combine(r[2], r[3], SEL), SEL),
+                           err_combine(err_combine(r[4], r[5], SEL), err_combine(r[6], r[7], SEL), SEL), SEL);
+      };
+      const float h6 = tree8(r6), h4 = tree8(r4);
+      const float sc6 = err_combine(h6, __shfl_xor_sync(0xFFFFFFFFu, h6, 16), SEL);
+      const float sc4 = err_combine(h4, __shfl_xor_sync(0xFFFFFFFFu, h4, 16), SEL);
+      const bool four = sc4 < sc6;  // strictly lower error: keep the max-4 candidate
+      if (four) s = s4;
+#pragma unroll
+      for (int p2 = 0; p2 < 4; ++p2) {
+        const uint32_t c0 = four ? code4[2 * p2] : code6[2 * p2], c1 = four ? code4[2 * p2 + 1] : code6[2 * p2 + 1];
+        store_row(2 * p2, c0);
+        store_row(2 * p2 + 1, c1);
+        interleave(p2, c0, c1);
+      }
+    } else {
+#pragma unroll
+      for (int p2 = 0; p2 < 4; ++p2) {
+        uint32_t code[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * p2 + h;
+          float z[8], v[8];
+          patch_row(pbase, pc, i, z);
+          if (SR) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = scaled<true>(z[j], s, 6.0f, word0_of(a, grow0 + i, gcol0 + j));
+          } else {
+            const float2 inv2 = make_float2(s.inv, s.inv);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 r = mul2(make_float2(z[2 * j], z[2 * j + 1]), inv2);
+              v[2 * j] = r.x;
+              v[2 * j + 1] = r.y;
+            }
+          }
+          code[h] = e2m1x8(v);
+          store_row(i, code[h]);
+        }
+        interleave(p2, code[0], code[1]);
+      }
     }
     if (COL) {
       uint32_t tl[4], th[4];
@@ -252,10 +300,10 @@ __global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) 
   }
 }
 
-template <bool ROW, bool COL, bool Q46, bool SR>
+template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
 cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
   constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStagePadBytes + tile::kSStagePadBytes + 16;  // + 2 barriers
-  auto kern = quant2d_kernel<ROW, COL, Q46, SR>;
+  auto kern = quant2d_kernel<ROW, COL, Q46, SR, SEL>;
   static int grid_cap[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -281,10 +329,17 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <bool ROW, bool COL, bool Q46, int SEL>
+cudaError_t launch_sr(const QuantArgs& a, bool sr, cudaStream_t st) {
+  return sr ? launch<ROW, COL, Q46, true, SEL>(a, st) : launch<ROW, COL, Q46, false, SEL>(a, st);
+}
+
 template <bool ROW, bool COL>
 cudaError_t launch_rc(const QuantArgs& a, bool q46, bool sr, cudaStream_t st) {
-  if (q46) return sr ? launch<ROW, COL, true, true>(a, st) : launch<ROW, COL, true, false>(a, st);
-  return sr ? launch<ROW, COL, false, true>(a, st) : launch<ROW, COL, false, false>(a, st);
+  if (!q46) return launch_sr<ROW, COL, false, kSelMAE>(a, sr, st);
+  if (a.sel == kSelMSE) return launch_sr<ROW, COL, true, kSelMSE>(a, sr, st);
+  if (a.sel == kSelMax) return launch_sr<ROW, COL, true, kSelMax>(a, sr, st);
+  return launch_sr<ROW, COL, true, kSelMAE>(a, sr, st);
 }
 
 }  // namespace
