@@ -112,7 +112,7 @@ __device__ __forceinline__ void transpose4x4(const uint32_t* w, uint32_t* t) {
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
-__global__ void __launch_bounds__(kBlockThreads, (Q46 && SR) ? 1 : ((Q46 || SR) ? 2 : 3))
+__global__ void __launch_bounds__(kBlockThreads, SR ? 2 : 3)
     quant2d_kernel(const QuantArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* bufs = smem;                                  // 2 x 32 KB tiles (1024-aligned)

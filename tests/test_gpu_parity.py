@@ -335,6 +335,21 @@ def test_counter_offset_reproduces_a_row_shard():
     assert np.array_equal(shard["s_col"], whole["s_col"][:, 8:])
 
 
+@pytest.mark.parametrize("offset", [(1 << 32) - 3000, (1 << 64) - 5000, (1 << 63) + 12345])
+@pytest.mark.parametrize("flags", [ROW | COL | SR, ROW | COL | TWO_D | SR, ROW | COL | F46 | SR])
+def test_counter_offsets_beyond_32_bits(offset, flags):
+    """Philox counters (element index + offset, as a 64-bit integer) whose low
+    word wraps inside the tensor, or whose 64-bit sum wraps, give the oracle's
+    bits: the high counter word is carried and the sum is taken modulo 2^64."""
+    bits = synthetic.activation_outlier_channels(128, 256, 61, frac=0.01)
+    x = to_device(bits)
+    g = gpu_quantize(x, flags, 0, sr_seed=0x5EEDF00D, counter_offset=offset)
+    r = ref_quantize(bits.view(np.uint16), flags, 0, sr_seed=0x5EEDF00D, counter_offset=offset)
+    assert_parity(g, r, flags)
+    base = gpu_quantize(x, flags, 0, sr_seed=0x5EEDF00D, counter_offset=0)
+    assert not np.array_equal(g["q_row"], base["q_row"])   # the offset reaches the rounding bits
+
+
 def test_deterministic_and_graph_capturable():
     bits = small_input()
     flags = ROW | COL | RHT_COL | SR
