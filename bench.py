@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -517,6 +518,88 @@ def run_oracle_sample(args, max_seconds: float = 20.0):
                       f"{done} rows ({elapsed:.2f} s), scaled to the full tensor"}
 
 
+def _oracle_stripe_worker(shm_name, shape, r0, r1, flags, sel, amax_parts, amax_all, idx, b_start, b_amax,
+                         b_quant, times):
+    """One process of the all-cores oracle run: amax of rows [r0, r1), then (after
+    the parent has reduced the stripes' maxima) the quantize of the same rows."""
+    from multiprocessing import shared_memory
+    import oracle
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        bits = np.ndarray(shape, dtype=np.uint16, buffer=shm.buf)
+        M, N = shape
+        outs = oracle.output_buffers(M, N, flags)
+        b_start.wait()
+        t0 = time.monotonic()
+        st, am = oracle.amax(bits[r0:r1], flags, synthetic.RHT_SEED)
+        amax_parts[2 * idx], amax_parts[2 * idx + 1] = float(am[0]), float(am[1])
+        b_amax.wait()
+        b_quant.wait()
+        am = np.array([amax_all[0], amax_all[1]], dtype=np.float32)
+        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
+                        row0=r0, row1=r1, outs=outs)
+        times[2 * idx], times[2 * idx + 1] = t0, time.monotonic()
+        del bits
+    finally:
+        shm.close()
+
+
+def run_oracle_all_cores(args):
+    """The oracle as it stands, run on every host core at once: the workload's
+    rows split into one stripe (a multiple of 16 rows) per process; each process
+    takes its stripe's amax, the parent reduces them, and each process then
+    quantizes its stripe.  Time = first start to last finish."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    import oracle
+
+    oracle.build()
+    flags, sel = workload_config(args)
+    bits = np.ascontiguousarray(synthetic.workload(args.workload).view(np.uint16))
+    M, N = bits.shape
+    n = max(1, min(len(os.sched_getaffinity(0)), M // 16))
+    blocks = M // 16
+    bounds = [16 * (blocks * i // n) for i in range(n)] + [M]
+    ctx = mp.get_context("spawn")
+    shm = shared_memory.SharedMemory(create=True, size=bits.nbytes)
+    try:
+        np.ndarray(bits.shape, dtype=np.uint16, buffer=shm.buf)[:] = bits
+        amax_parts = ctx.Array("f", 2 * n, lock=False)
+        amax_all = ctx.Array("f", 2, lock=False)
+        times = ctx.Array("d", 2 * n, lock=False)
+        b_start, b_amax, b_quant = ctx.Barrier(n + 1), ctx.Barrier(n + 1), ctx.Barrier(n + 1)
+        procs = [ctx.Process(target=_oracle_stripe_worker,
+                             args=(shm.name, bits.shape, bounds[i], bounds[i + 1], flags, sel, amax_parts, amax_all,
+                                   i, b_start, b_amax, b_quant, times)) for i in range(n)]
+        for p in procs:
+            p.start()
+        try:
+            b_start.wait(timeout=120)
+            b_amax.wait(timeout=120)
+            parts = np.frombuffer(amax_parts, dtype=np.float32).reshape(n, 2)
+            # NaN-propagating maximum, as a whole-tensor amax would give
+            amax_all[0], amax_all[1] = (float(np.max(parts[:, k])) for k in range(2))
+            b_quant.wait(timeout=120)
+        except threading.BrokenBarrierError:
+            pass
+        for p in procs:
+            p.join(timeout=120)
+            if p.exitcode is None:
+                p.kill()
+                p.join()
+        if any(p.exitcode != 0 for p in procs):
+            return None
+        t = np.frombuffer(times, dtype=np.float64).reshape(n, 2)
+        wall = float(t[:, 1].max() - t[:, 0].min())
+    finally:
+        shm.close()
+        shm.unlink()
+    nbytes = algorithmic_bytes(M, N, flags)
+    return {"value": round(nbytes / wall / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"the full {M}x{N} tensor (amax + quantize) in {n} processes over 16-row-aligned "
+                      f"row stripes, {wall:.2f} s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,6 +656,9 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = run_oracle_sample(args)
+            allc = run_oracle_all_cores(args)
+            if allc is not None:
+                res["cpu_baseline_all_cores"] = allc
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist
