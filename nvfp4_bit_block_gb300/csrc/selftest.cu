@@ -15,8 +15,13 @@
 // cap, how many differ at all, and the first differing byte case.
 //
 // A second hook runs the kernels' Hadamard transform alone, so that the
-// transformed values themselves can be compared with a reference.
+// transformed values themselves can be compared with a reference.  A third
+// compares the kernels' Philox4x32-10 (the stochastic-rounding words and the
+// RHT sign word) with cuRAND's device implementation of the same generator,
+// an independent one, over pseudo-random and extreme counters and keys.
 #include <cstdint>
+
+#include <curand_philox4x32_x.h>
 
 #include "nvfp4.h"
 #include "nvfp4_device.cuh"
@@ -165,6 +170,60 @@ NVFP4_API int nvfp4_test_rht(const void* x_dev, int64_t M, int64_t N, int64_t ld
   nvfp4::rht_check_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint16_t*>(x_dev), M, N, ld, along_cols, (uint32_t)rht_seed, (uint32_t)(rht_seed >> 32),
       out_dev);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// out[0] = counters whose words 0/1 differ from cuRAND's, out[1] = keys whose
+// 16 RHT sign bits (low half of word 0) differ, out[2] = cases checked.  Thread t of the grid takes
+// counter (c0, c1) and key (k0, k1) from a hash of t; the first 4096 threads
+// take counter and key words from {0, 1, 2^31, 2^32 - 1} instead, so that
+// carries and all-ones words are covered.
+__global__ void philox_check_kernel(unsigned long long* out) {
+  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t c0, c1, k0, k1;
+  if (t < 4096u) {
+    const uint32_t ext[4] = {0u, 1u, 0x80000000u, 0xFFFFFFFFu};
+    c0 = ext[t & 3u];
+    c1 = ext[(t >> 2) & 3u];
+    k0 = ext[(t >> 4) & 3u];
+    k1 = ext[(t >> 6) & 3u];
+    if (t >= 256u) {  // the rest: one extreme word, the others hashed
+      c0 ^= mix32(t * 0x9E3779B9u) & ((t >> 8) & 1u ? 0xFFFFFFFFu : 0u);
+      c1 ^= mix32(t * 0x85EBCA6Bu) & ((t >> 9) & 1u ? 0xFFFFFFFFu : 0u);
+      k0 ^= mix32(t * 0xC2B2AE35u) & ((t >> 10) & 1u ? 0xFFFFFFFFu : 0u);
+      k1 ^= mix32(t * 0x27D4EB2Fu) & ((t >> 11) & 1u ? 0xFFFFFFFFu : 0u);
+    }
+  } else {
+    c0 = mix32(t * 0x9E3779B9u + 1u);
+    c1 = mix32(t * 0x85EBCA6Bu + 2u);
+    k0 = mix32(t * 0xC2B2AE35u + 3u);
+    k1 = mix32(t * 0x27D4EB2Fu + 4u);
+  }
+  const uint2 ours = philox_w01(c0, c1, k0, k1);
+  const uint4 ref = curand_Philox4x32_10(make_uint4(c0, c1, 0u, 0u), make_uint2(k0, k1));
+  if (ours.x != ref.x || ours.y != ref.y) atomicAdd(out + 0, 1ull);
+  const uint4 ref_sign = curand_Philox4x32_10(make_uint4(0u, 0u, 0u, 1u), make_uint2(k0, k1));
+  if (rht_sign_bits(k0, k1) != (ref_sign.x & 0xFFFFu)) atomicAdd(out + 1, 1ull);  // 16 signs: low half of word 0
+  atomicAdd(out + 2, 1ull);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+// Test hook (not declared in nvfp4.h): compare the kernels' Philox4x32-10 with
+// cuRAND's over `blocks` x 256 counter/key cases (blocks >= 16 covers the
+// extreme words).  out_dev: three zeroed unsigned 64-bit counters (see above).
+NVFP4_API int nvfp4_test_philox_check(unsigned long long* out_dev, int blocks, void* stream) {
+  if (!out_dev) return NVFP4_ERR_NULL;
+  if (blocks <= 0) return NVFP4_ERR_SHAPE;
+  nvfp4::philox_check_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

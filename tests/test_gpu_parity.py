@@ -277,6 +277,22 @@ def test_scale_quotient_equals_ieee_division_exhaustively():
     assert bare > 0  # the bare product b * (1/den) alone is not enough
 
 
+def test_device_philox_equals_curand():
+    """The kernels' Philox4x32-10 (stochastic-rounding words 0 and 1, RHT sign
+    word) equals cuRAND's device implementation of the generator on 2^20
+    counter/key cases, including every combination of extreme words."""
+    import ctypes
+    hook = nv.lib().nvfp4_test_philox_check
+    hook.restype = ctypes.c_int
+    hook.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    assert hook(out.data_ptr(), 4096, None) == 0
+    torch.cuda.synchronize()
+    differ, differ_sign, checked = out.cpu().tolist()
+    assert checked == 4096 * 256
+    assert differ == 0 and differ_sign == 0
+
+
 def test_tile_copy_timeout_is_reported_and_the_context_stays_usable():
     """A 1D quantize whose tile copies never arrive (test hook: the tile
     barrier is armed but no copy is issued) stops after its bounded wait and
