@@ -2,6 +2,7 @@
 // translation units (not part of the public C ABI).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,6 +58,31 @@ struct HistArgs {
 constexpr int kBoxCols = 64;
 constexpr int kBoxRows = 64;
 cudaError_t make_tile_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t N, int64_t ld);
+
+// Grid of a persistent kernel on the current device: resident CTAs per SM
+// (at `threads` threads and `smem` bytes of dynamic shared memory, which the
+// kernel is first opted in to) times the SM count.  Computed once per device
+// and kept in `cache` (one 64-slot array per kernel instantiation; atomic, so
+// concurrent host threads may launch).
+template <typename Kernel>
+cudaError_t resident_grid(Kernel kern, int threads, int smem, std::atomic<int>* cache, int& cap) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool slot = dev >= 0 && dev < 64;
+  cap = slot ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (cap > 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  cap = (per_sm > 0 ? per_sm : 1) * sms;
+  if (slot) cache[dev].store(cap, std::memory_order_relaxed);
+  return cudaSuccess;
+}
 
 cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);

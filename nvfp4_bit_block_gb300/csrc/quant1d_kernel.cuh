@@ -444,21 +444,10 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   auto kern = quant1d_kernel<ROW, COL, Q46, SR, SEL, RHT>;
   // once per device: opt in to the dynamic shared memory and size the
   // persistent grid from the occupancy
-  static int grid_cap[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int cap = (dev >= 0 && dev < 64) ? grid_cap[dev] : 0;
-  if (cap == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockThreads, kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cap = (per_sm > 0 ? per_sm : 1) * sms;
-    if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
-  }
+  static std::atomic<int> grid_cap[64] = {};
+  int cap = 0;
+  const cudaError_t ge = resident_grid(kern, kBlockThreads, kSmem, grid_cap, cap);
+  if (ge != cudaSuccess) return ge;
   // persistent grid: every resident CTA slot, or one CTA per tile if fewer
   const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
   int64_t g = ntiles < cap ? ntiles : cap;

@@ -304,21 +304,10 @@ template <bool ROW, bool COL, bool Q46, bool SR, int SEL>
 cudaError_t launch(const QuantArgs& a, cudaStream_t st) {
   constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStagePadBytes + tile::kSStagePadBytes + 16;  // + 2 barriers
   auto kern = quant2d_kernel<ROW, COL, Q46, SR, SEL>;
-  static int grid_cap[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int cap = (dev >= 0 && dev < 64) ? grid_cap[dev] : 0;
-  if (cap == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockThreads, kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cap = (per_sm > 0 ? per_sm : 1) * sms;
-    if (dev >= 0 && dev < 64) grid_cap[dev] = cap;
-  }
+  static std::atomic<int> grid_cap[64] = {};
+  int cap = 0;
+  const cudaError_t ge = resident_grid(kern, kBlockThreads, kSmem, grid_cap, cap);
+  if (ge != cudaSuccess) return ge;
   const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
   int64_t grid = ntiles < cap ? ntiles : cap;
   if (grid < 1) grid = 1;

@@ -366,6 +366,47 @@ def test_counter_offsets_beyond_32_bits(offset, flags):
     assert not np.array_equal(g["q_row"], base["q_row"])   # the offset reaches the rounding bits
 
 
+def test_concurrent_host_threads_on_their_own_streams():
+    """Several host threads, each on its own stream, quantize at once (the
+    per-device launch caches are shared); every result equals the one-thread
+    result."""
+    import threading
+    bits = small_input(M=384, N=768)
+    x = to_device(bits)
+    cases = [(ROW | COL | F46, 2), (ROW | COL | TWO_D | SR, 0), (ROW | COL | RHT_COL | SR | F46, 1),
+             (COL | SR, 0), (ROW | RHT_ROW, 0), (ROW | COL | TWO_D | F46 | SR, 2)]
+    want = [gpu_quantize(x, f, sel, sr_seed=9, rht_seed=10) for f, sel in cases]
+    got = [None] * len(cases)
+    errors = []
+
+    def work(i):
+        try:
+            f, sel = cases[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    amax = nv.nvfp4_amax(x, f, 10, stream=st)
+                    out = nv.nvfp4_quantize(x, amax, f, sel, 9, 10, stream=st)
+                st.synchronize()
+            got[i] = out
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for w, g in zip(want, got):
+        for k in ("q_row", "s_row", "q_col", "s_col"):
+            t = getattr(g, k)
+            if w[k] is None:
+                assert t is None
+            else:
+                assert np.array_equal(t.cpu().numpy(), w[k]), k
+
+
 def test_deterministic_and_graph_capturable():
     bits = small_input()
     flags = ROW | COL | RHT_COL | SR
