@@ -94,6 +94,24 @@ def workload(name: str, M: int | None = None, N: int | None = None) -> np.ndarra
     return gen(M or M0, N or N0, seed)
 
 
+def tiled_large(M: int, N: int, seed: int, block_rows: int = 256) -> np.ndarray:
+    """A tensor too large to draw element by element in a test: a seeded
+    N(0,1) block of ``block_rows`` x N rows with outlier channels, repeated down
+    the rows, plus three seeded entries set to 40, 48 and 56 in the last rows
+    (so the tensor maximum lies beyond the first 2^31 elements)."""
+    block = activation_outlier_channels(block_rows, N, seed, frac=0.001, scale=8.0)
+    out = np.empty((M, N), dtype=np.uint16)
+    for r0 in range(0, M, block_rows):
+        r1 = min(M, r0 + block_rows)
+        out[r0:r1] = block[:r1 - r0]
+    rng = np.random.default_rng(seed + 1)
+    for v in (40.0, 48.0, 56.0):
+        r = int(rng.integers(max(0, M - 16), M))
+        c = int(rng.integers(0, N))
+        out[r, c] = _to_bf16_bits(np.array([v], np.float32))[0]
+    return out
+
+
 def workload_flags(name: str):
     """(flags, selection rule) of the named workload."""
     return WORKLOADS[name][4], WORKLOADS[name][5]

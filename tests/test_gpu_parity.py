@@ -435,6 +435,46 @@ def test_deterministic_and_graph_capturable():
 STRIPES = 6
 
 
+def assert_stripes_match_oracle(bits, g, flags, sel, stripes, sr_seed, rht_seed):
+    """GPU outputs of a whole tensor against the oracle on 16-row stripes."""
+    M, N = bits.shape
+    st, am = oracle.amax(bits, flags, rht_seed)
+    assert st == 0
+    outs = oracle.output_buffers(M, N, flags)
+    for sidx in stripes:
+        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=sr_seed, rht_seed=rht_seed,
+                        row0=16 * sidx, row1=16 * sidx + 16, outs=outs)
+    q_row, s_row, q_col, s_col = outs
+    rows = np.concatenate([np.arange(16 * s, 16 * s + 16) for s in stripes])
+    pick = lambda d, qr, sr, qc, sc: dict(
+        q_row=None if qr is None else qr[rows], s_row=None if sr is None else sr[rows],
+        q_col=None if qc is None else np.concatenate([qc[:, 8 * s:8 * s + 8] for s in stripes], 1),
+        s_col=None if sc is None else sc[:, stripes], **d)
+    gs = pick(dict(amax=g["amax"], alpha=g["alpha"], status=g["status"]),
+              g["q_row"], g["s_row"], g["q_col"], g["s_col"])
+    alpha = (am / np.float32(1536.0 if flags & F46 else 2688.0)).astype(np.float32)
+    rr = pick(dict(amax=am, alpha=alpha), q_row, s_row, q_col, s_col)
+    assert_parity(gs, rr, flags)
+
+
+@pytest.mark.parametrize("flags,sel", [(ROW | COL | SR, 0), (ROW | COL | F46, 1), (ROW | COL | TWO_D | F46 | SR, 0)])
+def test_more_than_two_to_the_31_elements(flags, sel):
+    """16400 x 131072 = 2.15e9 elements (4.3 GB of bf16): element indices,
+    output offsets and Philox counters beyond 2^31, the tensor maximum in the
+    last rows; stripes at both ends and across the 2^31 boundary are compared
+    with the oracle exactly."""
+    M, N = 16400, 131072
+    bits = synthetic.tiled_large(M, N, 77)
+    x = to_device(bits)
+    g = gpu_quantize(x, flags, sel, sr_seed=0xABCDEF, rht_seed=0)
+    del x
+    torch.cuda.empty_cache()
+    boundary = (1 << 31) // N // 16          # the stripe holding element 2^31
+    stripes = sorted(s for s in {0, 1, boundary - 1, boundary, boundary + 1, M // 16 - 1} if s < M // 16)
+    assert_stripes_match_oracle(bits, g, flags, sel, stripes, 0xABCDEF, 0)
+    assert float(g["amax"][0]) == 56.0
+
+
 @pytest.mark.parametrize("name", list(synthetic.WORKLOADS))
 def test_workload_full_size_sampled(name):
     flags, sel = synthetic.workload_flags(name)
