@@ -204,11 +204,15 @@ __device__ __forceinline__ uint32_t rht_sign_bits(uint32_t k0, uint32_t k1) {
 // Stochastic rounding of v onto the E2M1 grid with block maximum Q: with
 // m = min(|v|, Q) between grid neighbours lo <= m < hi, return hi iff
 // (w >> 8) * 2^-24 < (m - lo) / (hi - lo); the sign of v is kept.  All steps
-// are exact (power-of-two step sizes).
+// are exact (power-of-two step sizes).  The step hi - lo is 2^(e-1) for m in
+// [2^e, 2^(e+1)), e = 0, 1, 2, and 0.5 below 1: both it and its reciprocal
+// are formed on the exponent field (the step is max(2^e, 1) / 2; the
+// reciprocal's biased exponent is 254 minus the step's).
 __device__ __forceinline__ float sr_round(float v, float Q, uint32_t w) {
   const float m = fminf(fabsf(v), Q);
-  const float step = m < 2.0f ? 0.5f : (m < 4.0f ? 1.0f : 2.0f);
-  const float rstep = m < 2.0f ? 2.0f : (m < 4.0f ? 1.0f : 0.5f);
+  const uint32_t sb = max(__float_as_uint(m) & 0x7F800000u, 0x3F800000u) - 0x00800000u;
+  const float step = __uint_as_float(sb);
+  const float rstep = __uint_as_float(0x7F000000u - sb);
   const float lo = __fmul_rn(floorf(__fmul_rn(m, rstep)), step);
   const float p = __fmul_rn(__fsub_rn(m, lo), rstep);
   const float u = __fmul_rn((float)(w >> 8), 0x1p-24f);
