@@ -213,10 +213,13 @@ __device__ __forceinline__ float sr_round(float v, float Q, uint32_t w) {
   const uint32_t sb = max(__float_as_uint(m) & 0x7F800000u, 0x3F800000u) - 0x00800000u;
   const float step = __uint_as_float(sb);
   const float rstep = __uint_as_float(0x7F000000u - sb);
-  const float lo = __fmul_rn(floorf(__fmul_rn(m, rstep)), step);
-  const float p = __fmul_rn(__fsub_rn(m, lo), rstep);
+  // in units of the step: m / step = t, lo = f * step with f = floor(t), and
+  // the fraction p = t - f (every product and difference here is exact)
+  const float t = __fmul_rn(m, rstep);
+  const float f = floorf(t);
+  const float p = __fsub_rn(t, f);
   const float u = __fmul_rn((float)(w >> 8), 0x1p-24f);
-  const float g = (u < p) ? __fadd_rn(lo, step) : lo;
+  const float g = __fmul_rn((u < p) ? __fadd_rn(f, 1.0f) : f, step);
   return copysignf(g, v);
 }
 
