@@ -1,0 +1,59 @@
+"""The benchmark's host-side contract, on the CPU: the reference arm (the
+oracle timed on the host) prints one JSON line with the required keys, other
+ranks of a multi-rank launch print nothing, the algorithmic byte count is the
+metric's definition, and the all-cores oracle run covers the whole tensor."""
+import argparse
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def run_bench(*args, env=None):
+    e = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    if env:
+        e.update(env)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT, env=e)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [line for line in r.stdout.splitlines() if line.strip()]
+
+
+def test_reference_arm_prints_one_contract_line():
+    lines = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0")
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 0
+    assert d["config"]["workload"] == "act_46mae_8192x5120"
+    assert d["config"]["M"] == 8192 and d["config"]["N"] == 5120 and d["config"]["flags"] == 67
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert run_bench("--impl", "reference", "--steps", "1", "--warmup", "0", env={"RANK": "1"}) == []
+
+
+@pytest.mark.parametrize("flags,per_elem", [(1, 2.5625), (2, 2.5625), (3, 3.125), (3 | 4, 3.125), (1 | 64, 2.5625)])
+def test_algorithmic_bytes_are_the_metric_definition(flags, per_elem):
+    M, N = 8192, 5120
+    assert bench.algorithmic_bytes(M, N, flags) == int(per_elem * M * N)
+
+
+def test_all_cores_oracle_run_covers_the_tensor():
+    args = argparse.Namespace(workload="rowwise_rn_256x1024", flags=None, sel=None)
+    r = bench.run_oracle_all_cores(args)
+    assert r is not None
+    assert r["kind"] == "oracle" and r["value"] > 0
+    assert 1 <= r["cores"] <= min(len(os.sched_getaffinity(0)), 256 // 16)
+    assert "256x1024" in r["sample"]
