@@ -88,11 +88,25 @@ def _check(status: int, where: str) -> None:
         raise Nvfp4Error(status, where)
 
 
+def _on_device(device, **tensors) -> None:
+    """Every given tensor (None = absent) must live on `device`, a CUDA device:
+    the kernels dereference these pointers on that GPU."""
+    for name, t in tensors.items():
+        if t is not None and (not t.is_cuda or t.device != device):
+            raise ValueError(f"{name} must be a CUDA tensor on {device} (got {t.device})")
+
+
+def _outs(q):
+    return dict(q_row=q.q_row, s_row=q.s_row, q_col=q.q_col, s_col=q.s_col, alpha=q.alpha, status=q.status)
+
+
 def _matrix(x):
-    """(data_ptr, M, N, ld) of a 2-D bfloat16 tensor with unit column stride."""
+    """(data_ptr, M, N, ld) of a 2-D bfloat16 CUDA tensor with unit column stride."""
     import torch
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise TypeError("x must be a 2-D torch.bfloat16 tensor")
+    if not x.is_cuda:
+        raise ValueError(f"x must be a CUDA tensor (got {x.device})")
     if x.size(1) > 0 and x.stride(1) != 1:
         raise ValueError("x must have unit stride along columns")
     ld = x.stride(0) if x.size(0) > 1 else max(x.size(1), 8)
@@ -133,8 +147,10 @@ def nvfp4_amax(x, flags: int, rht_seed: int = 0, out=None, stream=None):
     p, M, N, ld = _matrix(x)
     if out is None:
         out = torch.empty(2, dtype=torch.float32, device=x.device)
-    _check(lib().nvfp4_amax(p, M, N, ld, flags, rht_seed, _ptr(out), _stream_handle(stream)),
-           "nvfp4_amax")
+    _on_device(x.device, out=out)
+    with torch.cuda.device(x.device):
+        _check(lib().nvfp4_amax(p, M, N, ld, flags, rht_seed, _ptr(out), _stream_handle(stream)),
+               "nvfp4_amax")
     return out
 
 
@@ -152,10 +168,12 @@ def nvfp4_quantize(x, amax, flags: int, sel: int = SEL_MAE, sr_seed: int = 0, rh
         out = Quantized(mk(q_row), mks(s_row), mk(q_col), mks(s_col),
                         alpha=torch.empty(2, dtype=torch.float32, device=x.device),
                         status=torch.zeros(1, dtype=torch.int32, device=x.device))
-    _check(lib().nvfp4_quantize(p, M, N, ld, _ptr(amax), flags, sel, sr_seed, rht_seed, counter_offset,
-                                _ptr(out.q_row), _ptr(out.s_row), _ptr(out.q_col), _ptr(out.s_col),
-                                _ptr(out.alpha), _ptr(out.status), _stream_handle(stream)),
-           "nvfp4_quantize")
+    _on_device(x.device, amax=amax, **_outs(out))
+    with torch.cuda.device(x.device):
+        _check(lib().nvfp4_quantize(p, M, N, ld, _ptr(amax), flags, sel, sr_seed, rht_seed, counter_offset,
+                                    _ptr(out.q_row), _ptr(out.s_row), _ptr(out.q_col), _ptr(out.s_col),
+                                    _ptr(out.alpha), _ptr(out.status), _stream_handle(stream)),
+               "nvfp4_quantize")
     return out
 
 
@@ -165,11 +183,15 @@ def nvfp4_dequantize(q, s, alpha, out_dtype=None, out=None, stream=None):
     import torch
     rows, half = q.shape
     cols = 2 * half
+    if not q.is_cuda:
+        raise ValueError(f"q must be a CUDA tensor (got {q.device})")
     if out is None:
         out = torch.empty((rows, cols), dtype=out_dtype or torch.float32, device=q.device)
+    _on_device(q.device, s=s, alpha=alpha, out=out)
     bf16 = 1 if out.dtype == torch.bfloat16 else 0
-    _check(lib().nvfp4_dequantize(_ptr(q), _ptr(s), _ptr(alpha), rows, cols, bf16, _ptr(out),
-                                  _stream_handle(stream)), "nvfp4_dequantize")
+    with torch.cuda.device(q.device):
+        _check(lib().nvfp4_dequantize(_ptr(q), _ptr(s), _ptr(alpha), rows, cols, bf16, _ptr(out),
+                                      _stream_handle(stream)), "nvfp4_dequantize")
     return out
 
 
@@ -182,6 +204,8 @@ def nvfp4_error_histogram(x, q_row, s_row, alpha, nbins: int = 24, out=None, str
     p, M, N, ld = _matrix(x)
     if out is None:
         out = torch.zeros((3, nbins), dtype=torch.int64, device=x.device)
-    _check(lib().nvfp4_error_histogram(p, M, N, ld, _ptr(q_row), _ptr(s_row), _ptr(alpha), nbins, _ptr(out),
-                                       _stream_handle(stream)), "nvfp4_error_histogram")
+    _on_device(x.device, q_row=q_row, s_row=s_row, alpha=alpha, out=out)
+    with torch.cuda.device(x.device):
+        _check(lib().nvfp4_error_histogram(p, M, N, ld, _ptr(q_row), _ptr(s_row), _ptr(alpha), nbins, _ptr(out),
+                                           _stream_handle(stream)), "nvfp4_error_histogram")
     return out

@@ -138,3 +138,21 @@ def test_error_histogram_rejects_bad_arguments(L):
 def test_binding_has_the_c_names():
     for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_error_histogram", "nvfp4_strerror"):
         assert callable(getattr(nv, name))
+
+
+def test_binding_rejects_host_tensors_before_any_launch():
+    """Host (CPU) tensors never reach the library: their addresses would be
+    dereferenced on the GPU."""
+    import torch
+    x = torch.zeros((32, 32), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        nv.nvfp4_amax(x, 3)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        nv.nvfp4_quantize(x, torch.zeros(2), 3)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        nv.nvfp4_error_histogram(x, None, None, None)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        nv.nvfp4_dequantize(torch.zeros((16, 8), dtype=torch.uint8), torch.zeros((16, 1), dtype=torch.uint8),
+                            torch.zeros(1))
+    with pytest.raises(TypeError):
+        nv.nvfp4_amax(torch.zeros((32, 32), dtype=torch.float32), 3)
