@@ -156,3 +156,23 @@ def test_binding_rejects_host_tensors_before_any_launch():
                             torch.zeros(1))
     with pytest.raises(TypeError):
         nv.nvfp4_amax(torch.zeros((32, 32), dtype=torch.float32), 3)
+
+
+def test_self_check_hooks_reject_bad_arguments(L):
+    """The GPU self-check hooks validate on the host before launching."""
+    ph = L.nvfp4_test_philox_check
+    ph.restype = ctypes.c_int
+    ph.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert ph(None, 16, None) == -1 and ph(ALIGNED, 0, None) == -2 and ph(ALIGNED, -3, None) == -2
+    qc = L.nvfp4_test_quotient_check
+    qc.restype = ctypes.c_int
+    qc.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert qc(None, None) == -1
+    rh = L.nvfp4_test_rht
+    rh.restype = ctypes.c_int
+    rh.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    assert rh(None, 16, 16, 16, 0, 0, ALIGNED, None) == -1
+    assert rh(ALIGNED, 16, 24, 24, 0, 0, ALIGNED2, None) == -2      # N % 16
+    assert rh(ALIGNED, 24, 16, 16, 1, 0, ALIGNED2, None) == -2      # along columns needs M % 16
+    assert rh(ALIGNED, 16, 16, 8, 0, 0, ALIGNED2, None) == -2       # ld < N
