@@ -488,12 +488,14 @@ def run_error_analysis(args, nbins: int = 24):
             "histogram_kernel_ms": round(e0.elapsed_time(e1), 4)}), flush=True)
 
 
-def run_oracle_sample(args, max_seconds: float = 20.0):
-    """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
+def run_oracle_sample(args, max_seconds: float = 20.0, bits=None):
+    """Time the CPU oracle (as it stands) on a bounded row sample of the
+    workload (`bits`: the workload's tensor if already drawn)."""
     import oracle
 
     flags, sel = workload_config(args)
-    bits = synthetic.workload(args.workload)
+    if bits is None:
+        bits = synthetic.workload(args.workload)
     M, N = bits.shape
     t0 = time.perf_counter()
     st, am = oracle.amax(bits, flags, synthetic.RHT_SEED)
@@ -634,10 +636,11 @@ def main():
             return
         per_step = []
         cb = None
+        bits = synthetic.workload(args.workload)  # drawn once; the steps time the oracle only
         for _ in range(args.warmup + args.steps):
-            cb = run_oracle_sample(args, max_seconds=4.0)
+            cb = run_oracle_sample(args, max_seconds=4.0, bits=bits)
             per_step.append(cb["value"])
-        v = statistics.mean(per_step[args.warmup:]) if args.steps else per_step[-1]
+        v = round(statistics.mean(per_step[args.warmup:]) if args.steps else per_step[-1], 5)
         flags, sel = workload_config(args)
         _, M, N = synthetic.WORKLOADS[args.workload][:3]
         print(json.dumps({
