@@ -1,12 +1,10 @@
 // api.cu -- the C ABI declared in include/nvfp4.h: host-side argument
 // validation, flag decoding and kernel dispatch.  Nothing here allocates
-// memory or keeps state (apart from two one-shot test hooks); every call
-// enqueues work on the caller's stream.
+// memory or keeps state; every call enqueues work on the caller's stream.
 #include "nvfp4.h"
 
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
 #include "nvfp4_internal.h"
@@ -38,17 +36,7 @@ int check_shape(int64_t M, int64_t N, int64_t ld, uint32_t flags) {
   return NVFP4_OK;
 }
 
-// Test hook: when set, the next launch reports a CUDA failure without
-// enqueueing anything (exercises the NVFP4_ERR_CUDA path on any machine).
-std::atomic<int> g_fail_next_launch{0};
-// Test hook: the next 1D quantize arms its tile barriers but issues no copy,
-// so its bounded waits run out and it reports NVFP4_ERR_PIPELINE.
-std::atomic<int> g_skip_next_copy{0};
-
-int launch_status(cudaError_t e) {
-  if (g_fail_next_launch.exchange(0)) return NVFP4_ERR_CUDA;
-  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
-}
+int launch_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 }  // namespace
 
@@ -62,7 +50,6 @@ int nvfp4_amax(const void* x_dev, int64_t M, int64_t N, int64_t ld, uint32_t fla
   if (st) return st;
   if (!amax_dev || (!x_dev && M > 0 && N > 0)) return NVFP4_ERR_NULL;
   if (!aligned(amax_dev, 4) || (x_dev && !aligned(x_dev, 16))) return NVFP4_ERR_ALIGN;
-  if (g_fail_next_launch.load()) return launch_status(cudaSuccess);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(amax_dev, 0, 2 * sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (M == 0 || N == 0) return NVFP4_OK;
@@ -122,9 +109,7 @@ int nvfp4_quantize(const void* x_dev, int64_t M, int64_t N, int64_t ld, const fl
   a.rht_row = (flags & NVFP4_RHT_ROW) ? 1 : 0;
   a.rht_col = (flags & NVFP4_RHT_COL) ? 1 : 0;
   a.sf_swz = (flags & NVFP4_SF_SWIZZLED) ? 1 : 0;
-  a.test_skip_copy = g_skip_next_copy.exchange(0);
   const bool q46 = (flags & NVFP4_46) != 0, sr = (flags & NVFP4_SR) != 0;
-  if (g_fail_next_launch.load()) return launch_status(cudaSuccess);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (flags & NVFP4_2D) return launch_status(nvfp4::launch_quant2d(a, row, col, q46, sr, s));
   return launch_status(nvfp4::launch_quant1d(a, row, col, q46, sr, s));
@@ -136,7 +121,6 @@ int nvfp4_dequantize(const uint8_t* q_dev, const uint8_t* s_dev, const float* al
   if (rows == 0 || cols == 0) return NVFP4_OK;
   if (!q_dev || !s_dev || !alpha_dev || !out_dev) return NVFP4_ERR_NULL;
   if (!aligned(q_dev, 8) || !aligned(alpha_dev, 4) || !aligned(out_dev, 16)) return NVFP4_ERR_ALIGN;
-  if (g_fail_next_launch.load()) return launch_status(cudaSuccess);
   nvfp4::DequantArgs a;
   a.q = q_dev;
   a.s = s_dev;
@@ -158,7 +142,6 @@ int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int64_t ld, c
   if (!x_dev || !q_dev || !s_dev || !alpha_dev) return NVFP4_ERR_NULL;
   if (!aligned(x_dev, 16) || ld % 8 || !aligned(q_dev, 8) || !aligned(alpha_dev, 4) || !aligned(hist_dev, 8))
     return NVFP4_ERR_ALIGN;
-  if (g_fail_next_launch.load()) return launch_status(cudaSuccess);
   nvfp4::HistArgs a;
   a.x = static_cast<const uint16_t*>(x_dev);
   a.M = M;
@@ -186,14 +169,5 @@ const char* nvfp4_strerror(int status) {
     default: return "unknown status";
   }
 }
-
-// Test hook (not declared in nvfp4.h): make the next launch report
-// NVFP4_ERR_CUDA without enqueueing anything.
-NVFP4_API void nvfp4_test_fail_next_launch(void) { g_fail_next_launch.store(1); }
-
-// Test hook (not declared in nvfp4.h): the next 1D nvfp4_quantize issues no
-// tile copy, so it stops after its bounded wait with NVFP4_ERR_PIPELINE in
-// status_dev.
-NVFP4_API void nvfp4_test_skip_next_copy(void) { g_skip_next_copy.store(1); }
 
 }  // extern "C"

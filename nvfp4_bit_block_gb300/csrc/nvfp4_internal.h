@@ -24,8 +24,7 @@ struct QuantArgs {
   uint32_t rht_k0, rht_k1;
   int sel;
   int rht_row, rht_col;
-  int sf_swz;          // scales in the tiled block-scaled-MMA layout
-  int test_skip_copy;  // test hook: arm the first tile's barrier but issue no copy
+  int sf_swz;  // scales in the tiled block-scaled-MMA layout
 };
 
 struct AmaxArgs {

@@ -1,4 +1,8 @@
-// selftest.cu -- exhaustive device check of the scale-byte quotient.
+// nvfp4_selftest.cu -- device self-checks of the quantizer's building blocks,
+// built into a test-only library (libnvfp4_selftest.so) that the tests load;
+// the product library holds none of this code.
+//
+// Exhaustive device check of the scale-byte quotient.
 //
 // The quantize kernels take E4M3(fl(b / den)) from scale_byte (quotient_rn:
 // a product and one residual correction, capped at 1e6) instead of an IEEE
@@ -18,13 +22,20 @@
 // transformed values themselves can be compared with a reference.  A third
 // compares the kernels' Philox4x32-10 (the stochastic-rounding words and the
 // RHT sign word) with cuRAND's device implementation of the same generator,
-// an independent one, over pseudo-random and extreme counters and keys.
+// an independent one, over pseudo-random and extreme counters and keys.  A
+// fourth launches the 1D quantize kernel in a variant that arms its tile
+// barriers but issues no copy, so that the bounded wait runs out.
 #include <cstdint>
 
 #include <curand_philox4x32_x.h>
 
 #include "nvfp4.h"
 #include "nvfp4_device.cuh"
+#include "quant1d_kernel.cuh"
+
+namespace {
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+}  // namespace
 
 namespace nvfp4 {
 namespace {
@@ -100,6 +111,7 @@ extern "C" {
 // out_dev: six zeroed unsigned 64-bit counters on the device (see above).
 NVFP4_API int nvfp4_test_quotient_check(unsigned long long* out_dev, void* stream) {
   if (!out_dev) return NVFP4_ERR_NULL;
+  if (!aligned(out_dev, 8)) return NVFP4_ERR_ALIGN;
   const dim3 grid(nvfp4::kLastA - nvfp4::kFirstA + 1, 6);
   nvfp4::quotient_check_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
@@ -160,11 +172,12 @@ extern "C" {
 
 // Test hook (not declared in nvfp4.h): the kernels' Hadamard transform of a
 // bf16 M x N tensor (row stride ld, 4-byte aligned rows), 16-vectors along
-// rows or columns, into a dense fp32 M x N buffer.
+// rows or columns, into a dense fp32 M x N buffer (4-byte aligned).
 NVFP4_API int nvfp4_test_rht(const void* x_dev, int64_t M, int64_t N, int64_t ld, int along_cols, uint64_t rht_seed,
                              float* out_dev, void* stream) {
   if (!x_dev || !out_dev) return NVFP4_ERR_NULL;
-  if (M <= 0 || N <= 0 || N % 16 || ld < N || ld % 2 || (along_cols && M % 16)) return NVFP4_ERR_SHAPE;
+  if (M <= 0 || N <= 0 || N % 16 || ld < N || (along_cols && M % 16)) return NVFP4_ERR_SHAPE;
+  if (ld % 2 || !aligned(x_dev, 4) || !aligned(out_dev, 4)) return NVFP4_ERR_ALIGN;
   const int64_t nv = along_cols ? (M / 16) * (N / 2) : M * (N / 16);
   const int64_t grid = (nv + 255) / 256;
   nvfp4::rht_check_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
@@ -222,9 +235,45 @@ extern "C" {
 // extreme words).  out_dev: three zeroed unsigned 64-bit counters (see above).
 NVFP4_API int nvfp4_test_philox_check(unsigned long long* out_dev, int blocks, void* stream) {
   if (!out_dev) return NVFP4_ERR_NULL;
+  if (!aligned(out_dev, 8)) return NVFP4_ERR_ALIGN;
   if (blocks <= 0) return NVFP4_ERR_SHAPE;
   nvfp4::philox_check_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+// Test hook: the rowwise + columnwise round-to-nearest 1D quantize kernel in
+// a variant whose tile barriers are armed but whose copies are never issued,
+// so every wait runs out: the kernel writes NVFP4_ERR_PIPELINE to status_dev
+// after about a second and returns.  Arguments as nvfp4_quantize with flags
+// ROWWISE | COLWISE; all pointers are required.
+NVFP4_API int nvfp4_test_quantize_no_copy(const void* x_dev, int64_t M, int64_t N, int64_t ld, const float* amax_dev,
+                                          uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                          float* alpha_dev, int* status_dev, void* stream) {
+  if (!x_dev || !amax_dev || !q_row || !s_row || !q_col || !s_col || !alpha_dev || !status_dev) return NVFP4_ERR_NULL;
+  if (M <= 0 || N <= 0 || M % 16 || N % 16 || ld < N || M > INT32_MAX || N > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (ld % 8 || !aligned(x_dev, 16) || !aligned(q_row, 16) || !aligned(q_col, 16) || !aligned(s_row, 4) ||
+      !aligned(s_col, 4) || !aligned(amax_dev, 4) || !aligned(alpha_dev, 4) || !aligned(status_dev, 4))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::QuantArgs a{};
+  a.x = static_cast<const uint16_t*>(x_dev);
+  a.M = M;
+  a.N = N;
+  a.ld = ld;
+  a.amax = amax_dev;
+  a.alpha = alpha_dev;
+  a.status = status_dev;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.sel = nvfp4::kSelMAE;
+  const cudaError_t e =
+      nvfp4::q1d::launch<true, true, false, false, nvfp4::kSelMAE, 0, true>(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // extern "C"
