@@ -1,15 +1,27 @@
 """Benchmark of the NVFP4 quantizer hot path on one GB300 (or N replicas).
 
-A step is one pass of the whole hot path over one tensor: nvfp4_amax (tensor
-amax per copy) then nvfp4_quantize (scale, round, pack; rowwise + transposed
-columnwise outputs).  The default workload is the recipe's activation tensor,
-8192 x 5120 bf16 with outlier channels, 4/6 with MAE selection, both copies.
+A step is one pass of the whole hot path over every tensor of the workload:
+for each tensor nvfp4_amax (tensor amax per copy) then nvfp4_quantize (scale,
+round, pack; rowwise + transposed columnwise outputs).  The default workload
+is the recipe's full linear layer (its largest configuration):
+
+  X  16384 x 5120  activation, 1x16 blocks, 4/6 with MSE selection, both copies
+  W  5120 x 20480  weight, 16x16 2D blocks, both copies
+  dY 16384 x 20480 gradient, Hadamard on the columnwise copy, stochastic
+                   rounding on both copies
+
+The single tensors (the 256x1024 rowwise case, the 8192x5120 activation, the
+weight, the 16384x5120 gradient, and each linear-layer tensor alone) are
+available with --workload.
 
 Metric: NVFP4 quantize GB/s = (bf16 bytes read + code bytes + scale bytes
-written) per step / step time.  The timed steps rotate over several input and
-output sets whose combined size exceeds the L2, so every step reads from HBM.
-The roofline entry is for the dominant kernel (quantize), timed with CUDA
-events on its own stream inside the same rotating stream of steps.
+written) per step / step time.  The timed steps rotate over input/output sets
+whose combined size exceeds the L2, so every step reads from HBM.  Every kernel
+is also timed alone inside the same rotating stream (CUDA events on its own
+stream); the roofline entry is for the kernel that takes the most time: HBM
+bandwidth for the codec kernels, and for the stochastic-rounding kernels
+(one Philox4x32-10 call per element, bound by 32x32->64-bit integer products)
+Philox calls per second against the SMs' wide-multiply rate.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
   python bench.py --report | --error-analysis | --once
@@ -22,12 +34,12 @@ cores instead (a bounded row sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -40,13 +52,49 @@ import synthetic  # noqa: E402
 METRIC = "NVFP4 quantize GB/s (bf16 in + fp4/scales out), % of GB300 HBM peak"
 UNIT = "GB/s"
 
-
-# DRAM bytes (read + written) of one quantize launch, from one ncu capture of
-# the current kernel on that workload (cold cache; outputs partly still in L2
-# at kernel end).  Keyed by (workload, flags, selection); absent -> null.
-QUANTIZE_TRAFFIC_BYTES = {
-    ("act_46mae_8192x5120", 67, 0): 83_940_864 + 10_233_856,
+# Workloads made of several tensors quantized in one step.
+COMPOSITES = {
+    "linear_layer": ["linear_x_16384x5120", "linear_w_5120x20480", "linear_dy_16384x20480"],
 }
+DEFAULT_WORKLOAD = "linear_layer"
+WORKLOAD_CHOICES = list(COMPOSITES) + list(synthetic.WORKLOADS)
+
+# Integer-multiply roofline of the stochastic-rounding kernels: a Philox4x32-10
+# call takes ten rounds of two 32x32->64-bit products; with the counter's
+# upper words zero, the first round's second product is a product with zero
+# and the last round's first product feeds only the unused words 2 and 3, so
+# 18 products per call depend on the counter.  A 64-bit-result integer
+# multiply issues at a quarter of the 128 lanes per clock of an SM (measured:
+# 28.7-29.7 products per clock per SM for mul.wide.u32 and mul.hi.u32).
+PHILOX_PRODUCTS_PER_CALL = 18
+WIDE_PRODUCTS_PER_CLK_PER_SM = 32
+
+# DRAM bytes (read + written) of one launch of a kernel from an ncu capture,
+# keyed by (tensor, kernel) with the hash of the kernel sources the capture was
+# taken on; a stale hash reports null.
+TRAFFIC = {}
+CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources of the product library (16 hex digits)."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(part: str, kernel: str):
+    entry = TRAFFIC.get((part, kernel))
+    if entry is None or entry[1] != source_hash():
+        return None
+    return entry[0]
+
+
+def parts_of(workload: str):
+    return COMPOSITES.get(workload, [workload])
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -67,12 +115,18 @@ def algorithmic_bytes(M: int, N: int, flags: int) -> int:
 
 
 def measured_peaks():
+    """(HBM GB/s, kind, SM max MHz) from MEASURED_PEAKS.json, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
+    return 6800.0, "fallback", 2070.0
+
+
+def philox_peak_gcalls(sms: int, sm_mhz: float) -> float:
+    """Philox calls per second (G) at the SMs' wide-multiply rate."""
+    return sms * WIDE_PRODUCTS_PER_CLK_PER_SM / PHILOX_PRODUCTS_PER_CALL * sm_mhz * 1e6 / 1e9
 
 
 class ClockSampler:
@@ -124,6 +178,46 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(args, part: str):
+    """(flags, selection) of one tensor of the workload (--flags/--sel override)."""
+    flags, sel = synthetic.workload_flags(part)
+    if getattr(args, "flags", None) is not None:
+        flags = args.flags
+    if getattr(args, "sel", None) is not None:
+        sel = args.sel
+    return flags, sel
+
+
+def _kernel_roofline(part, kernel, flags, M, N, ms, hbm_peak, peak_kind, sms, sm_mhz):
+    """Roofline record of one kernel launch that took `ms` on average."""
+    if kernel == "amax":
+        nbytes = 2 * M * N
+        rec = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+               "algorithmic": f"{nbytes} bytes (bf16 read)"}
+    elif flags & 32:  # stochastic rounding: one Philox4x32-10 call per element
+        calls = M * N
+        rec = {"bound": "alu", "achieved": calls / (ms * 1e-3) / 1e9, "peak": round(philox_peak_gcalls(sms, sm_mhz), 1),
+               "unit": "G Philox calls/s",
+               "algorithmic": f"{calls} Philox4x32-10 calls x {PHILOX_PRODUCTS_PER_CALL} wide products",
+               "peak_basis": f"{sms} SMs x {WIDE_PRODUCTS_PER_CLK_PER_SM} 32x32->64 products/clk / "
+                             f"{PHILOX_PRODUCTS_PER_CALL} per call x {sm_mhz:.0f} MHz",
+               "hbm_gbs": round(algorithmic_bytes(M, N, flags) / (ms * 1e-3) / 1e9, 1)}
+    else:
+        nbytes = algorithmic_bytes(M, N, flags)
+        rec = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+               "algorithmic": f"{nbytes} bytes (bf16 read + codes + scales)"}
+    rec["achieved"] = round(rec["achieved"], 1)
+    rec["frac"] = round(rec["achieved"] / rec["peak"], 4)
+    rec["peak_kind"] = peak_kind if rec["bound"] == "hbm" else "derived from the SM count, the measured " \
+                                                                 "multiply rate and the maximum SM clock"
+    t = traffic_of(part, kernel)
+    rec["traffic"] = t
+    if t is not None:
+        rec["dram_gbs"] = round(t / (ms * 1e-3) / 1e9, 1)
+    rec.update({"kernel": kernel, "tensor": part, "ms": round(ms, 5)})
+    return rec
+
+
 def run_ours(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -136,35 +230,52 @@ def run_ours(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     nv.lib()
-    flags, sel = workload_config(args)
-    bits = synthetic.workload(args.workload)
-    M, N = bits.shape
-    x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    parts = parts_of(args.workload)
+    cfg = []
+    for p in parts:
+        flags, sel = workload_config(args, p)
+        bits = synthetic.workload(p)
+        M, N = bits.shape
+        host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        cfg.append(dict(part=p, flags=flags, sel=sel, M=M, N=N, host=host, nbytes=algorithmic_bytes(M, N, flags)))
+        del bits
+    nbytes = sum(c["nbytes"] for c in cfg)
     # Several input/output sets used in rotation, so that the bytes touched
     # between two uses of the same set exceed the 129 MB L2: every step reads
-    # its input from HBM and the previous steps' outputs are written back
+    # its inputs from HBM and the previous steps' outputs are written back
     # during later steps, as in a steady stream of tensors.
-    per_set = algorithmic_bytes(M, N, flags)
-    nsets = max(2, -(-3 * 128 * 2**20 // per_set))
+    nsets = max(2, -(-3 * 128 * 2**20 // nbytes))
     stream = torch.cuda.Stream(device=dev)
-    xs = [x_host.to(dev) for _ in range(nsets)]
-    amaxs = [torch.empty(2, dtype=torch.float32, device=dev) for _ in range(nsets)]
-    outs = [nv.nvfp4_quantize(xs[i], nv.nvfp4_amax(xs[i], flags, synthetic.RHT_SEED), flags, sel)
-            for i in range(nsets)]
+    sets = []
+    for i in range(nsets):
+        s = []
+        for c in cfg:
+            x = c["host"].to(dev)
+            am = torch.empty(2, dtype=torch.float32, device=dev)
+            out = nv.nvfp4_quantize(x, nv.nvfp4_amax(x, c["flags"], synthetic.RHT_SEED), c["flags"], c["sel"])
+            s.append((x, am, out))
+        sets.append(s)
     torch.cuda.synchronize()
-    x, amax, out = xs[0], amaxs[0], outs[0]
 
-    def step(i):
-        nv.nvfp4_amax(xs[i], flags, synthetic.RHT_SEED, out=amaxs[i], stream=stream)
-        nv.nvfp4_quantize(xs[i], amaxs[i], flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, 0, out=outs[i],
-                          stream=stream)
+    def step(i, events=None):
+        for j, c in enumerate(cfg):
+            x, am, out = sets[i][j]
+            if events is not None:
+                events[j][0].record(stream)
+            nv.nvfp4_amax(x, c["flags"], synthetic.RHT_SEED, out=am, stream=stream)
+            if events is not None:
+                events[j][1].record(stream)
+            nv.nvfp4_quantize(x, am, c["flags"], c["sel"], synthetic.SR_SEED, synthetic.RHT_SEED, 0, out=out,
+                              stream=stream)
+            if events is not None:
+                events[j][2].record(stream)
 
     with torch.cuda.stream(stream):
         for k in range(max(args.warmup, nsets)):
             step(k % nsets)
     torch.cuda.synchronize()
 
-    # the step (amax then quantize) as one CUDA graph per set: no host launch gaps
+    # the step (every amax and quantize) as one CUDA graph per set: no host launch gaps
     graphs = []
     for i in range(nsets):
         g = torch.cuda.CUDAGraph()
@@ -177,14 +288,22 @@ def run_ours(args, rank: int, world: int):
             graphs[k % nsets].replay()
     torch.cuda.synchronize()
 
+    def timed_interval(nsteps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(nsteps):
+                graphs[k % nsets].replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    # the timed steps last milliseconds, shorter than the sampling interval, so
-    # the sampler also covers an untimed half second of the same steps run
-    # right before them: the clocks reported are the clocks under this load
+    # The sampler also covers untimed steps run right before the timed ones
+    # (at least half a second), so the clocks reported are the clocks under
+    # this load even when the timed region is shorter than its interval.
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for k in range(max(1, 2 * nsets)):
@@ -192,6 +311,7 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.synchronize()
     per_step_s = max((time.perf_counter() - t0) / max(1, 2 * nsets), 1e-6)
     load_steps = int(min(20000, max(1, 0.5 / per_step_s)))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         time.sleep(0.06)  # the sampler's first reading precedes the load
         with torch.cuda.stream(stream):
@@ -202,41 +322,36 @@ def run_ours(args, rank: int, world: int):
                 graphs[k % nsets].replay()
             ev1.record(stream)
         torch.cuda.synchronize()
+        # further intervals of the same length, for the spread of the figure
+        repeats = [timed_interval(args.steps) for _ in range(5)]
     if world > 1:
         dist.barrier()
     total_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
 
-    # per-kernel durations inside the same rotating stream of steps, launched
-    # directly with an event between the two kernels, for the roofline of the
-    # dominant kernel
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Every kernel timed alone inside the same rotating stream of steps:
+    # the calls are launched directly with an event between any two.
+    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in cfg] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for k in range(args.steps):
-            i = k % nsets
-            kev[k][0].record(stream)
-            nv.nvfp4_amax(xs[i], flags, synthetic.RHT_SEED, out=amaxs[i], stream=stream)
-            kev[k][1].record(stream)
-            nv.nvfp4_quantize(xs[i], amaxs[i], flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, 0, out=outs[i],
-                              stream=stream)
-            kev[k][2].record(stream)
+            step(k % nsets, kev[k])
     torch.cuda.synchronize()
-    amax_ms = [e[0].elapsed_time(e[1]) for e in kev]
-    quant_ms = [e[1].elapsed_time(e[2]) for e in kev]
-    for o in outs:
-        status = int(o.status.item())
-        assert status == 0, f"quantize reported status {status}"
+    for s in sets:
+        for _, _, out in s:
+            status = int(out.status.item())
+            assert status == 0, f"quantize reported status {status}"
 
-    # End to end through the public API: every step copies its input from
-    # pinned host memory to the device, runs amax + quantize and copies all
-    # outputs back to pinned host memory.  Steps are pipelined the way a
+    # End to end through the public API: every step copies its inputs from
+    # pinned host memory to the device, runs amax + quantize on each and copies
+    # all outputs back to pinned host memory.  Steps are pipelined the way a
     # stream of tensors would be: copy-in, compute and copy-out run on their
-    # own streams, ordered by events, over two device buffer sets (the input
-    # and output of set i are reused two steps later).
-    e2e_steps = max(4, min(args.steps, 12))
+    # own streams, ordered by events, over two device buffer sets (the inputs
+    # and outputs of set i are reused two steps later).
+    e2e_steps = max(4, min(args.steps, 8))
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    dev_outs = [[t_ for t_ in (o.q_row, o.s_row, o.q_col, o.s_col, o.alpha) if t_ is not None] for o in outs[:2]]
+    dev_outs = [[t_ for (_, _, o) in sets[i] for t_ in (o.q_row, o.s_row, o.q_col, o.s_col, o.alpha) if t_ is not None]
+                for i in range(2)]
     host_outs = [[torch.empty(t_.shape, dtype=t_.dtype, pin_memory=True) for t_ in d] for d in dev_outs]
-    x_hosts = [x_host, x_host.clone().pin_memory()]
+    x_hosts = [[c["host"] for c in cfg], [c["host"].clone().pin_memory() for c in cfg]]
     ev_in = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
     ev_comp = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
     ev_out = [torch.cuda.Event() for _ in range(e2e_steps + 2)]
@@ -246,8 +361,9 @@ def run_ours(args, rank: int, world: int):
         i = k % 2
         with torch.cuda.stream(s_in):
             if k >= 2:
-                s_in.wait_event(ev_comp[k - 2])     # set i's input no longer read
-            xs[i].copy_(x_hosts[i], non_blocking=True)
+                s_in.wait_event(ev_comp[k - 2])     # set i's inputs no longer read
+            for j in range(len(cfg)):
+                sets[i][j][0].copy_(x_hosts[i][j], non_blocking=True)
             ev_in[k].record(s_in)
         with torch.cuda.stream(stream):
             stream.wait_event(ev_in[k])
@@ -270,63 +386,79 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     d2h = sum(t_.numel() * t_.element_size() for t_ in dev_outs[0])
+    h2d = sum(2 * c["M"] * c["N"] for c in cfg)
 
-    nbytes = algorithmic_bytes(M, N, flags)
+    hbm_peak, peak_kind, sm_max_mhz = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kernels = []
+    for j, c in enumerate(cfg):
+        am_ms = statistics.mean(e[j][0].elapsed_time(e[j][1]) for e in kev)
+        q_ms = statistics.mean(e[j][1].elapsed_time(e[j][2]) for e in kev)
+        kernels.append(_kernel_roofline(c["part"], "amax", c["flags"], c["M"], c["N"], am_ms, hbm_peak, peak_kind,
+                                        sms, sm_max_mhz))
+        kernels.append(_kernel_roofline(c["part"], "quantize", c["flags"], c["M"], c["N"], q_ms, hbm_peak, peak_kind,
+                                        sms, sm_max_mhz))
+    dominant = max(kernels, key=lambda r: r["ms"])
     value = nbytes * args.steps / (total_ms * 1e-3) / 1e9 * world
-    peak, peak_kind = measured_peaks()
-    quant_avg_ms = statistics.mean(quant_ms)
-    achieved = nbytes / (quant_avg_ms * 1e-3) / 1e9
+    clk = clocks.summary()
+    ms_per_step = total_ms / args.steps
+    if len(parts) == 1:
+        c = cfg[0]
+        config = {"workload": parts[0], "M": c["M"], "N": c["N"], "flags": c["flags"], "selection": c["sel"]}
+    else:
+        config = {"workload": args.workload,
+                  "tensors": [{"name": c["part"], "M": c["M"], "N": c["N"], "flags": c["flags"], "selection": c["sel"]}
+                              for c in cfg]}
+    config.update({"elements": sum(c["M"] * c["N"] for c in cfg), "bytes_per_step": nbytes,
+                   "l2": f"inputs larger than L2: {nsets} input/output sets of {nbytes / 1e6:.0f} MB in rotation",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"})
+    reps = sorted(r / args.steps for r in repeats)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16->nvfp4 (fp32 arithmetic)",
-        "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "flags": flags, "selection": sel,
-                   "elements": M * N, "bytes_per_step": nbytes,
-                   "l2": f"inputs larger than L2: {nsets} input/output sets of {per_set / 1e6:.0f} MB in rotation",
-                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
-        "kernels_ms": {"amax": round(statistics.mean(amax_ms), 5), "quantize": round(quant_avg_ms, 5)},
-        "elements_per_s": round(M * N * args.steps * world / (total_ms * 1e-3), 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": QUANTIZE_TRAFFIC_BYTES.get((args.workload, flags, sel)), "peak_kind": peak_kind,
-                     "kernel": "quantize"},
-        "step_frac_of_peak": round(value / world / peak, 4),
+        "data": "synthetic (seeded, the recipe's shapes and value distributions)",
+        "config": config,
+        "kernels_ms": {f"{r['tensor']}:{r['kernel']}": r["ms"] for r in kernels},
+        "elements_per_s": round(config["elements"] * args.steps * world / (total_ms * 1e-3), 1),
+        "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+        "roofline_detail": dominant,
+        "kernels": kernels,
+        "step_frac_of_hbm_peak": round(value / world / hbm_peak, 4),
+        "repeat_intervals": {"count": len(reps), "ms_per_step_median": round(statistics.median(reps), 5),
+                             "ms_per_step_min": round(reps[0], 5), "ms_per_step_max": round(reps[-1], 5)},
         "e2e": {"value": round(nbytes / e2e_s / 1e9 * world, 1), "unit": UNIT,
-                "h2d_bytes_per_step": 2 * M * N, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
-        "step": "CUDA graph replay of nvfp4_amax (memset + kernel) then nvfp4_quantize",
-        "clocks": clocks.summary(),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * len(cfg) * args.steps,
+        "step": "CUDA graph replay of nvfp4_amax (memset + kernel) then nvfp4_quantize for each tensor",
+        "clocks": clk,
     }
+    if clk.get("sm_mhz"):
+        res["ms_x_sm_mhz"] = round(ms_per_step * clk["sm_mhz"], 2)
     return res
 
 
-def workload_config(args):
-    flags, sel = synthetic.workload_flags(args.workload)
-    if getattr(args, "flags", None) is not None:
-        flags = args.flags
-    if getattr(args, "sel", None) is not None:
-        sel = args.sel
-    return flags, sel
-
-
 def run_once(args):
-    """Three amax + quantize passes on one workload, nothing timed: the
-    command the ncu captures under profiles/ run."""
+    """Three amax + quantize passes over each tensor of the workload, nothing
+    timed: the command the ncu captures under profiles/ run."""
     import torch
 
     import nvfp4_bit_block_gb300 as nv
 
     nv.lib()
-    flags, sel = workload_config(args)
-    bits = synthetic.workload(args.workload)
-    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
-    for _ in range(3):
-        amax = nv.nvfp4_amax(x, flags, synthetic.RHT_SEED)
-        out = nv.nvfp4_quantize(x, amax, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED)
-    torch.cuda.synchronize()
-    assert int(out.status.item()) == 0
-    print(json.dumps({"once": args.workload, "flags": flags, "selection": sel}))
+    for p in parts_of(args.workload):
+        flags, sel = workload_config(args, p)
+        bits = synthetic.workload(p)
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+        del bits
+        for _ in range(3):
+            amax = nv.nvfp4_amax(x, flags, synthetic.RHT_SEED)
+            out = nv.nvfp4_quantize(x, amax, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED)
+        torch.cuda.synchronize()
+        assert int(out.status.item()) == 0
+        print(json.dumps({"once": p, "flags": flags, "selection": sel}))
+        del x, out
+        torch.cuda.empty_cache()
 
 
 def _time_kernels(nv, torch, xs, flags, sel, reps):
@@ -380,7 +512,7 @@ def _report_line(kind, name, M, N, flags, sel, amax_ms, quant_ms, step_ms, peak)
 
 
 def run_report(args):
-    """One JSON line per measurement: every recipe workload, the 4/6, RHT and
+    """One JSON line per measurement: every recipe tensor, the 4/6, RHT and
     SR ablations, and the size sweep of the activation (X) path from 2^20 to
     2^30 elements.  Input/output sets rotate so that each step reads from HBM.
     amax_us / quantize_us time each call alone (its input cold in L2);
@@ -390,7 +522,7 @@ def run_report(args):
     import nvfp4_bit_block_gb300 as nv
 
     nv.lib()
-    peak, _ = measured_peaks()
+    peak = measured_peaks()[0]
     reps = max(5, args.steps)
 
     def sets_of(bits_or_tensor, M, N, flags):
@@ -418,6 +550,8 @@ def run_report(args):
                  ("act_46mae_8192x5120", "4/6 MAE", 67, 0), ("act_46mae_8192x5120", "4/6 MSE", 67, 1),
                  ("act_46mae_8192x5120", "4/6 MAXERR", 67, 2), ("act_46mae_8192x5120", "RN rowwise only", 1, 0),
                  ("act_46mae_8192x5120", "4/6 MAE rowwise only", 65, 0),
+                 ("act_46mae_8192x5120", "RN columnwise only", 2, 0),
+                 ("act_46mae_8192x5120", "4/6 MAE columnwise only", 66, 0),
                  ("grad_rht_sr_16384x5120", "RN", 3, 0), ("grad_rht_sr_16384x5120", "RHT(col)", 19, 0),
                  ("grad_rht_sr_16384x5120", "SR", 35, 0), ("grad_rht_sr_16384x5120", "RHT(col)+SR", 51, 0),
                  ("weight_2d_5120x20480", "1D RN", 3, 0), ("weight_2d_5120x20480", "2D RN", 7, 0),
@@ -455,7 +589,8 @@ def run_error_analysis(args, nbins: int = 24):
     import torch
     import nvfp4_bit_block_gb300 as nv
     nv.build()
-    bits = synthetic.workload(args.workload)
+    name = parts_of(args.workload)[0] if args.workload in COMPOSITES else args.workload
+    bits = synthetic.workload(name)
     M, N = bits.shape
     x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
     lo = int(4 * nbins / 6)
@@ -479,7 +614,7 @@ def run_error_analysis(args, nbins: int = 24):
         bins = [[round(6 * i / nbins, 4), round(6 * (i + 1) / nbins, 4), int(cnt[i]), round(float(mean[i]), 5),
                  round(float(rms[i]), 5)] for i in range(nbins)]
         print(json.dumps({
-            "analysis": "error_histogram", "workload": args.workload, "M": M, "N": N, "variant": label,
+            "analysis": "error_histogram", "workload": name, "M": M, "N": N, "variant": label,
             "flags": flags, "selection": sel, "copy": "rowwise",
             "bins [v_lo, v_hi, count, mean e, rms e]": bins,
             "mean_e_v_4_to_6": round(float(se[lo:].sum() / max(cnt[lo:].sum(), 1)), 5),
@@ -488,118 +623,76 @@ def run_error_analysis(args, nbins: int = 24):
             "histogram_kernel_ms": round(e0.elapsed_time(e1), 4)}), flush=True)
 
 
-def run_oracle_sample(args, max_seconds: float = 20.0, bits=None):
-    """Time the CPU oracle (as it stands) on a bounded row sample of the
-    workload (`bits`: the workload's tensor if already drawn)."""
+def run_oracle_sample(args, max_seconds: float = 20.0, bits_by_part=None):
+    """The CPU oracle (as it stands, one thread) on a bounded row sample of
+    every tensor of the workload, scaled to the whole step: per tensor the
+    amax over a leading row stripe and the quantize of a growing number of
+    leading rows, each scaled by the tensor's row count.  `bits_by_part`: the
+    tensors if already drawn."""
     import oracle
 
-    flags, sel = workload_config(args)
-    if bits is None:
-        bits = synthetic.workload(args.workload)
-    M, N = bits.shape
-    t0 = time.perf_counter()
-    st, am = oracle.amax(bits, flags, synthetic.RHT_SEED)
-    t_amax = time.perf_counter() - t0
-    rows = 16
-    outs = oracle.output_buffers(M, N, flags)
-    elapsed = 0.0
-    done = 0
-    while elapsed < max_seconds / 2 and done < M:
-        n = min(rows, M - done)
+    parts = parts_of(args.workload)
+    total_bytes = 0
+    t_step = 0.0
+    notes = []
+    for p in parts:
+        flags, sel = workload_config(args, p)
+        bits = bits_by_part[p] if bits_by_part else synthetic.workload(p)
+        M, N = bits.shape
+        nb = algorithmic_bytes(M, N, flags)
+        total_bytes += nb
+        budget = max_seconds * nb / sum(algorithmic_bytes(*synthetic.WORKLOADS[q][1:3], workload_config(args, q)[0])
+                                        for q in parts)
+        arows = min(M, 256)
         t0 = time.perf_counter()
-        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
-                        row0=done, row1=done + n, outs=outs)
-        elapsed += time.perf_counter() - t0
-        done += n
-        rows = min(rows * 2, 1024)
-    frac = done / M
-    t_step = t_amax + elapsed / frac           # full-tensor estimate: amax + scaled quantize
-    nbytes = algorithmic_bytes(M, N, flags)
-    return {"value": round(nbytes / t_step / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"amax over the full {M}x{N} tensor ({t_amax:.2f} s) + quantize of the first "
-                      f"{done} rows ({elapsed:.2f} s), scaled to the full tensor"}
-
-
-def _oracle_stripe_worker(shm_name, shape, r0, r1, flags, sel, amax_parts, amax_all, idx, b_start, b_amax,
-                         b_quant, times):
-    """One process of the all-cores oracle run: amax of rows [r0, r1), then (after
-    the parent has reduced the stripes' maxima) the quantize of the same rows."""
-    from multiprocessing import shared_memory
-    import oracle
-    shm = shared_memory.SharedMemory(name=shm_name)
-    try:
-        bits = np.ndarray(shape, dtype=np.uint16, buffer=shm.buf)
-        M, N = shape
+        st, _ = oracle.amax(bits[:arows], flags, synthetic.RHT_SEED)
+        t_amax = (time.perf_counter() - t0) * M / arows
+        st, am = oracle.amax(bits[:arows], flags, synthetic.RHT_SEED)  # the sample's amax scales the sample
         outs = oracle.output_buffers(M, N, flags)
-        b_start.wait()
-        t0 = time.monotonic()
-        st, am = oracle.amax(bits[r0:r1], flags, synthetic.RHT_SEED)
-        amax_parts[2 * idx], amax_parts[2 * idx + 1] = float(am[0]), float(am[1])
-        b_amax.wait()
-        b_quant.wait()
-        am = np.array([amax_all[0], amax_all[1]], dtype=np.float32)
-        oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
-                        row0=r0, row1=r1, outs=outs)
-        times[2 * idx], times[2 * idx + 1] = t0, time.monotonic()
-        del bits
-    finally:
-        shm.close()
+        elapsed, done, rows = 0.0, 0, 16
+        while elapsed < budget / 2 and done < M:
+            n = min(rows, M - done)
+            t0 = time.perf_counter()
+            oracle.quantize(bits, N, am, flags, sel=sel, sr_seed=synthetic.SR_SEED, rht_seed=synthetic.RHT_SEED,
+                            row0=done, row1=done + n, outs=outs)
+            elapsed += time.perf_counter() - t0
+            done += n
+            rows = min(rows * 2, 1024)
+        t_step += t_amax + elapsed * M / done
+        notes.append(f"{p}: amax of {arows} rows, quantize of {done} rows of {M}")
+        del outs
+    return {"value": round(total_bytes / t_step / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "; ".join(notes) + "; each scaled to the whole tensor"}
 
 
 def run_oracle_all_cores(args):
-    """The oracle as it stands, run on every host core at once: the workload's
-    rows split into one stripe (a multiple of 16 rows) per process; each process
-    takes its stripe's amax, the parent reduces them, and each process then
-    quantizes its stripe.  Time = first start to last finish."""
-    import multiprocessing as mp
-    from multiprocessing import shared_memory
-    import oracle
+    """The oracle as it stands, run on every host core at once over the whole
+    workload: each tensor's rows split into one stripe (a multiple of 16 rows)
+    per process, each process takes its stripe's amax, the parent reduces
+    them, and each process then quantizes its stripe.  Time = the amax and
+    quantize phases of every tensor, first start to last finish."""
+    from oracle.parallel import amax_parallel, quantize_parallel
 
-    oracle.build()
-    flags, sel = workload_config(args)
-    bits = np.ascontiguousarray(synthetic.workload(args.workload).view(np.uint16))
-    M, N = bits.shape
-    n = max(1, min(len(os.sched_getaffinity(0)), M // 16))
-    blocks = M // 16
-    bounds = [16 * (blocks * i // n) for i in range(n)] + [M]
-    ctx = mp.get_context("spawn")
-    shm = shared_memory.SharedMemory(create=True, size=bits.nbytes)
-    try:
-        np.ndarray(bits.shape, dtype=np.uint16, buffer=shm.buf)[:] = bits
-        amax_parts = ctx.Array("f", 2 * n, lock=False)
-        amax_all = ctx.Array("f", 2, lock=False)
-        times = ctx.Array("d", 2 * n, lock=False)
-        b_start, b_amax, b_quant = ctx.Barrier(n + 1), ctx.Barrier(n + 1), ctx.Barrier(n + 1)
-        procs = [ctx.Process(target=_oracle_stripe_worker,
-                             args=(shm.name, bits.shape, bounds[i], bounds[i + 1], flags, sel, amax_parts, amax_all,
-                                   i, b_start, b_amax, b_quant, times)) for i in range(n)]
-        for p in procs:
-            p.start()
-        try:
-            b_start.wait(timeout=120)
-            b_amax.wait(timeout=120)
-            parts = np.frombuffer(amax_parts, dtype=np.float32).reshape(n, 2)
-            # NaN-propagating maximum, as a whole-tensor amax would give
-            amax_all[0], amax_all[1] = (float(np.max(parts[:, k])) for k in range(2))
-            b_quant.wait(timeout=120)
-        except threading.BrokenBarrierError:
-            pass
-        for p in procs:
-            p.join(timeout=120)
-            if p.exitcode is None:
-                p.kill()
-                p.join()
-        if any(p.exitcode != 0 for p in procs):
+    total_bytes, wall, procs = 0, 0.0, 0
+    for p in parts_of(args.workload):
+        flags, sel = workload_config(args, p)
+        bits = np.ascontiguousarray(synthetic.workload(p).view(np.uint16))
+        M, N = bits.shape
+        t0 = time.monotonic()
+        st, am = amax_parallel(bits, flags, synthetic.RHT_SEED)
+        t_amax = time.monotonic() - t0
+        if st != 0:
             return None
-        t = np.frombuffer(times, dtype=np.float64).reshape(n, 2)
-        wall = float(t[:, 1].max() - t[:, 0].min())
-    finally:
-        shm.close()
-        shm.unlink()
-    nbytes = algorithmic_bytes(M, N, flags)
-    return {"value": round(nbytes / wall / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
-            "sample": f"the full {M}x{N} tensor (amax + quantize) in {n} processes over 16-row-aligned "
-                      f"row stripes, {wall:.2f} s"}
+        r = quantize_parallel(bits, flags, sel, synthetic.SR_SEED, synthetic.RHT_SEED, amax2=am)
+        if r["status"] != 0:
+            return None
+        wall += t_amax + r["seconds"]
+        procs = max(procs, r["procs"])
+        total_bytes += algorithmic_bytes(M, N, flags)
+        del bits, r
+    return {"value": round(total_bytes / wall / 1e9, 4), "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"the whole workload ({', '.join(parts_of(args.workload))}): amax and quantize in {procs} "
+                      f"processes over 16-row-aligned row stripes, {wall:.2f} s"}
 
 
 def main():
@@ -607,18 +700,20 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="act_46mae_8192x5120", choices=list(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_CHOICES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--flags", type=int, default=None, help="override the workload's flags")
-    ap.add_argument("--sel", type=int, default=None, help="override the workload's 4/6 selection rule")
+    ap.add_argument("--flags", type=int, default=None, help="override the flags (single-tensor workloads)")
+    ap.add_argument("--sel", type=int, default=None, help="override the 4/6 selection rule (single-tensor workloads)")
     ap.add_argument("--once", action="store_true",
-                    help="run amax + quantize three times on the workload and exit (for profilers)")
+                    help="run amax + quantize three times on each tensor and exit (for profilers)")
     ap.add_argument("--report", action="store_true",
-                    help="print one JSON line per workload, ablation and X-path size (2^20..2^30)")
+                    help="print one JSON line per tensor, ablation and X-path size (2^20..2^30)")
     ap.add_argument("--error-analysis", action="store_true",
                     help="print the rowwise error histogram over the scaled value, standard vs 4/6")
     args = ap.parse_args()
+    if args.workload in COMPOSITES and (args.flags is not None or args.sel is not None):
+        ap.error("--flags / --sel apply to single-tensor workloads")
     if args.error_analysis:
         run_error_analysis(args)
         return
@@ -636,17 +731,25 @@ def main():
             return
         per_step = []
         cb = None
-        bits = synthetic.workload(args.workload)  # drawn once; the steps time the oracle only
+        drawn = {p: synthetic.workload(p) for p in parts_of(args.workload)}  # drawn once; the steps time the oracle
         for _ in range(args.warmup + args.steps):
-            cb = run_oracle_sample(args, max_seconds=4.0, bits=bits)
+            cb = run_oracle_sample(args, max_seconds=4.0, bits_by_part=drawn)
             per_step.append(cb["value"])
         v = round(statistics.mean(per_step[args.warmup:]) if args.steps else per_step[-1], 5)
-        flags, sel = workload_config(args)
-        _, M, N = synthetic.WORKLOADS[args.workload][:3]
+        parts = parts_of(args.workload)
+        if len(parts) == 1:
+            flags, sel = workload_config(args, parts[0])
+            _, M, N = synthetic.WORKLOADS[parts[0]][:3]
+            config = {"workload": parts[0], "M": M, "N": N, "flags": flags, "selection": sel}
+        else:
+            config = {"workload": args.workload,
+                      "tensors": [{"name": p, "M": synthetic.WORKLOADS[p][1], "N": synthetic.WORKLOADS[p][2],
+                                   "flags": workload_config(args, p)[0], "selection": workload_config(args, p)[1]}
+                                  for p in parts]}
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "config": {"workload": args.workload, "M": M, "N": N, "flags": flags, "selection": sel},
+            "config": config,
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))

@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4ref_error_histogram.restype = c.c_int
         L.nvfp4ref_error_histogram.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p,
                                                c.c_float, c.c_int, c.c_void_p]
+        L.nvfp4ref_gemm.restype = c.c_int
+        L.nvfp4ref_gemm.argtypes = [c.c_void_p, c.c_void_p, c.c_float, c.c_void_p, c.c_void_p, c.c_float,
+                                    c.c_int64, c.c_int64, c.c_int64, c.c_void_p]
         L.nvfp4ref_dequantize.restype = c.c_int
         L.nvfp4ref_dequantize.argtypes = [c.c_void_p, c.c_void_p, c.c_float, c.c_int64, c.c_int64,
                                           c.c_int, c.c_void_p]
@@ -245,3 +248,18 @@ def error_histogram(x_bf16: np.ndarray, N: int, q_row: np.ndarray, s_row: np.nda
     st = lib().nvfp4ref_error_histogram(_ptr(x), M, N, ld, _ptr(q), _ptr(s), float(alpha), nbins, _ptr(hist))
     assert st == OK, st
     return hist
+
+
+def gemm(qa: np.ndarray, sa: np.ndarray, alpha_a: float, qb: np.ndarray, sb: np.ndarray, alpha_b: float,
+         K: int) -> np.ndarray:
+    """D = A * B^T (float32 M x N) of NVFP4 operands with plain scales:
+    qa M x K/2 codes, sa M x K/16 scales; qb N x K/2, sb N x K/16."""
+    a = np.ascontiguousarray(qa, dtype=np.uint8)
+    b = np.ascontiguousarray(qb, dtype=np.uint8)
+    xa = np.ascontiguousarray(sa, dtype=np.uint8)
+    xb = np.ascontiguousarray(sb, dtype=np.uint8)
+    M, N = a.shape[0], b.shape[0]
+    d = np.zeros((M, N), dtype=np.float32)
+    st = lib().nvfp4ref_gemm(_ptr(a), _ptr(xa), float(alpha_a), _ptr(b), _ptr(xb), float(alpha_b), M, N, K, _ptr(d))
+    assert st == OK, st
+    return d

@@ -541,3 +541,39 @@ int nvfp4ref_error_histogram(const uint16_t* x, int64_t M, int64_t N, int64_t ld
     }
   return REF_OK;
 }
+
+/* NVFP4 GEMM of two operands in the layout the quantizer writes ("NVFP4
+ * revolutionizes AI training" headline page: Blackwell computes matrix
+ * products (GEMM) on FP4 operands natively).  A is M x K, B is N x K, both
+ * with 16-element blocks along K (codes M x K/2 and N x K/2 bytes, plain
+ * scales M x K/16 and N x K/16); D = A * B^T, M x N floats.
+ * Reading: each operand is dequantized exactly as nvfp4ref_dequantize forms
+ * it (x^ = val(q) * (e4m3(s) * alpha), rounded to float), the products and
+ * their sum over k are formed in double, and each element is rounded once to
+ * float. */
+int nvfp4ref_gemm(const uint8_t* qa, const uint8_t* sa, float alpha_a, const uint8_t* qb,
+                  const uint8_t* sb, float alpha_b, int64_t M, int64_t N, int64_t K, float* d) {
+  if (M < 0 || N < 0 || K < 0 || K % 16) return REF_ERR_SHAPE;
+  if (M == 0 || N == 0) return REF_OK;
+  if (!d || (K > 0 && (!qa || !sa || !qb || !sb))) return REF_ERR_NULL;
+  float* xa = (float*)malloc(sizeof(float) * (size_t)(M * (K > 0 ? K : 1)));
+  float* xb = (float*)malloc(sizeof(float) * (size_t)(N * (K > 0 ? K : 1)));
+  if (!xa || !xb) {
+    free(xa);
+    free(xb);
+    return REF_ERR_NULL;
+  }
+  if (K > 0) {
+    nvfp4ref_dequantize(qa, sa, alpha_a, M, K, 0, xa);
+    nvfp4ref_dequantize(qb, sb, alpha_b, N, K, 0, xb);
+  }
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += (double)xa[m * K + k] * (double)xb[n * K + k];
+      d[m * N + n] = (float)acc;
+    }
+  free(xa);
+  free(xb);
+  return REF_OK;
+}

@@ -98,6 +98,11 @@ int nvfp4ref_quantize(const uint16_t* x, int64_t M, int64_t N, int64_t ld, const
 int nvfp4ref_dequantize(const uint8_t* q, const uint8_t* s, float alpha, int64_t rows,
                         int64_t cols, int out_is_bf16, void* out);
 
+/* D = A * B^T of two NVFP4 operands (A: M x K, B: N x K, plain scales),
+ * each dequantized as above, products summed in double, rounded once. */
+int nvfp4ref_gemm(const uint8_t* qa, const uint8_t* sa, float alpha_a, const uint8_t* qb,
+                  const uint8_t* sb, float alpha_b, int64_t M, int64_t N, int64_t K, float* d);
+
 /* Error histogram of a rowwise copy over v = 6|x|/b (see the definition). */
 int nvfp4ref_error_histogram(const uint16_t* x, int64_t M, int64_t N, int64_t ld, const uint8_t* q,
                              const uint8_t* s, float alpha, int nbins, uint64_t* hist);

@@ -26,8 +26,33 @@ def run_bench(*args, env=None):
     return [line for line in r.stdout.splitlines() if line.strip()]
 
 
+def test_default_workload_is_the_full_linear_layer():
+    """The default step is the recipe's largest configuration: X (4/6-MSE),
+    W (2D) and dY (Hadamard on the columnwise copy + SR), both copies each."""
+    assert bench.DEFAULT_WORKLOAD == "linear_layer"
+    parts = bench.parts_of("linear_layer")
+    assert parts == ["linear_x_16384x5120", "linear_w_5120x20480", "linear_dy_16384x20480"]
+    import synthetic
+    assert [synthetic.WORKLOADS[p][1:3] for p in parts] == [(16384, 5120), (5120, 20480), (16384, 20480)]
+    assert [synthetic.workload_flags(p) for p in parts] == [(1 | 2 | 64, 1), (1 | 2 | 4, 0), (1 | 2 | 16 | 32, 0)]
+    total = sum(bench.algorithmic_bytes(*synthetic.WORKLOADS[p][1:3], synthetic.workload_flags(p)[0]) for p in parts)
+    assert total == 262_144_000 + 327_680_000 + 1_048_576_000
+
+
+def test_philox_roofline_peak_from_unit_counts():
+    """152 SMs x 32 wide products per clock / 18 products per call x 2070 MHz."""
+    assert abs(bench.philox_peak_gcalls(152, 2070.0) - 152 * 32 / 18 * 2.07) < 1e-9
+
+
+def test_traffic_is_null_for_a_stale_capture(monkeypatch):
+    monkeypatch.setattr(bench, "TRAFFIC", {("t", "quantize"): (123, "0" * 16)})
+    assert bench.traffic_of("t", "quantize") is None
+    monkeypatch.setattr(bench, "TRAFFIC", {("t", "quantize"): (123, bench.source_hash())})
+    assert bench.traffic_of("t", "quantize") == 123
+
+
 def test_reference_arm_prints_one_contract_line():
-    lines = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0")
+    lines = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "act_46mae_8192x5120")
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference"

@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_gemm_oracle as gemm_pins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
@@ -41,6 +42,14 @@ MUTATIONS = [
     ("no_clamp_to_q", "float m = fminf(fabsf(v), (float)Q);", "float m = fabsf(v);"),
     ("sign_dropped", "codes[i] = (uint8_t)((sign << 3) | idx);", "codes[i] = (uint8_t)idx;"),
     ("scale_uses_q6_always", "float den = (float)Q * alpha;", "float den = 6.0f * alpha;"),
+    ("gemm_b_uses_a_scales", "nvfp4ref_dequantize(qb, sb, alpha_b, N, K, 0, xb);",
+     "nvfp4ref_dequantize(qb, sa, alpha_b, N, K, 0, xb);"),
+    ("gemm_b_k_reversed", "acc += (double)xa[m * K + k] * (double)xb[n * K + k];",
+     "acc += (double)xa[m * K + k] * (double)xb[n * K + (K - 1 - k)];"),
+    ("gemm_drops_alpha_b", "nvfp4ref_dequantize(qb, sb, alpha_b, N, K, 0, xb);",
+     "nvfp4ref_dequantize(qb, sb, 1.0f, N, K, 0, xb);"),
+    ("gemm_float_accumulator", "double acc = 0.0;\n      for (int64_t k = 0; k < K; ++k) acc +=",
+     "float acc = 0.0f;\n      for (int64_t k = 0; k < K; ++k) acc +="),
     ("2d_scale_not_replicated", "if (do_col) s_col[(tc + k) * (M / 16) + tr / 16] = e;", "if (do_col) s_col[(tc + k) * (M / 16) + tr / 16] = (uint8_t)(e + (k == 3));"),
 ]
 
@@ -56,6 +65,8 @@ PIN_FUNCS = [
     pins.test_philox_known_answers, pins.test_sr_edge_cases, pins.test_zero_tensor,
     pins.test_2d_copies_are_transposes_and_dequantize_identically,
     pins.test_row_stripes_and_counter_offset_reproduce_the_whole,
+    gemm_pins.test_gemm_equals_the_exact_rational_sum, gemm_pins.test_gemm_is_bilinear_in_scales_and_signs,
+    gemm_pins.test_gemm_transpose_symmetry_and_reduction_order,
 ]
 FLAG_SAMPLE = [1, 3, 3 | 64, 7, 3 | 16, 3 | 32, 3 | 16 | 32, 1 | 8 | 32 | 64, 7 | 32, 7 | 64]
 
