@@ -10,6 +10,7 @@ The functions keep the C names:
 * :func:`nvfp4_amax`       -- float32[2] tensor amax (rowwise copy, columnwise copy)
 * :func:`nvfp4_quantize`   -- packed E2M1 codes + E4M3 scales (+ alpha) per copy
 * :func:`nvfp4_dequantize` -- codes + scales + alpha -> float32 or bfloat16
+* :func:`nvfp4_gemm`       -- D = alpha_a * alpha_b * A * B^T of two NVFP4 operands (tiled scales)
 * :func:`nvfp4_strerror`
 """
 from __future__ import annotations
@@ -25,7 +26,7 @@ from .build import build
 __all__ = [
     "ROWWISE", "COLWISE", "TWO_D", "RHT_ROW", "RHT_COL", "SR", "FOUR_SIX",
     "SEL_MAE", "SEL_MSE", "SEL_MAXERR", "Nvfp4Error", "Quantized", "lib", "build",
-    "nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_strerror", "output_shapes",
+    "nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_gemm", "nvfp4_strerror", "output_shapes",
 ]
 
 ROWWISE, COLWISE, TWO_D, RHT_ROW, RHT_COL, SR, FOUR_SIX, SF_SWIZZLED = 1, 2, 4, 8, 16, 32, 64, 128
@@ -62,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_error_histogram.restype = c.c_int
         L.nvfp4_error_histogram.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p,
                                             c.c_void_p, c.c_int, c.c_void_p, c.c_void_p]
+        L.nvfp4_gemm.restype = c.c_int
+        L.nvfp4_gemm.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
+                                 c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p]
         L.nvfp4_strerror.restype = c.c_char_p
         L.nvfp4_strerror.argtypes = [c.c_int]
         _lib = L
@@ -208,4 +212,26 @@ def nvfp4_error_histogram(x, q_row, s_row, alpha, nbins: int = 24, out=None, str
     with torch.cuda.device(x.device):
         _check(lib().nvfp4_error_histogram(p, M, N, ld, _ptr(q_row), _ptr(s_row), _ptr(alpha), nbins, _ptr(out),
                                            _stream_handle(stream)), "nvfp4_error_histogram")
+    return out
+
+
+def nvfp4_gemm(qa, sfa, alpha_a, qb, sfb, alpha_b, out=None, status=None, stream=None):
+    """D (float32, M x N) = alpha_a * alpha_b * A * B^T: qa (M x K/2) / qb (N x K/2)
+    codes with K contiguous, sfa / sfb their scales in the tiled layout
+    (NVFP4_SF_SWIZZLED), alpha_a / alpha_b one-element device views of the
+    copies' alpha."""
+    import torch
+    M, half = qa.shape
+    N = qb.shape[0]
+    K = 2 * half
+    if qb.shape[1] != half:
+        raise ValueError("A and B must have the same K")
+    if not qa.is_cuda:
+        raise ValueError(f"qa must be a CUDA tensor (got {qa.device})")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    _on_device(qa.device, sfa=sfa, alpha_a=alpha_a, qb=qb, sfb=sfb, alpha_b=alpha_b, out=out, status=status)
+    with torch.cuda.device(qa.device):
+        _check(lib().nvfp4_gemm(_ptr(qa), _ptr(sfa), _ptr(alpha_a), _ptr(qb), _ptr(sfb), _ptr(alpha_b), M, N, K,
+                                _ptr(out), out.stride(0), _ptr(status), _stream_handle(stream)), "nvfp4_gemm")
     return out

@@ -24,7 +24,7 @@ SELFTEST_BUILD = os.path.join(SELFTEST_DIR, "_build")
 SELFTEST_LIB = os.path.join(SELFTEST_BUILD, "libnvfp4_selftest.so")
 
 SOURCES = ["api.cu", "tmap.cu", "amax.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
-           "quant2d.cu", "dequant.cu", "analysis.cu"]
+           "quant2d.cu", "dequant.cu", "analysis.cu", "gemm.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

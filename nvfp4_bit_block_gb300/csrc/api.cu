@@ -155,6 +155,34 @@ int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int64_t ld, c
   return launch_status(nvfp4::launch_error_hist(a, static_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4_gemm(const uint8_t* qa_dev, const uint8_t* sfa_dev, const float* alpha_a_dev, const uint8_t* qb_dev,
+               const uint8_t* sfb_dev, const float* alpha_b_dev, int64_t M, int64_t N, int64_t K, float* d_dev,
+               int64_t ldd, int* status_dev, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || M % 128 || N % 128 || K % 256 || ldd < N) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (K == 0) return NVFP4_ERR_SHAPE;
+  if (!qa_dev || !sfa_dev || !alpha_a_dev || !qb_dev || !sfb_dev || !alpha_b_dev || !d_dev) return NVFP4_ERR_NULL;
+  if (!aligned(qa_dev, 16) || !aligned(qb_dev, 16) || !aligned(sfa_dev, 16) || !aligned(sfb_dev, 16) ||
+      !aligned(d_dev, 16) || ldd % 4 || !aligned(alpha_a_dev, 4) || !aligned(alpha_b_dev, 4) ||
+      (status_dev && !aligned(status_dev, 4)))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::GemmArgs a;
+  a.qa = qa_dev;
+  a.sfa = sfa_dev;
+  a.alpha_a = alpha_a_dev;
+  a.qb = qb_dev;
+  a.sfb = sfb_dev;
+  a.alpha_b = alpha_b_dev;
+  a.d = d_dev;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldd = ldd;
+  a.status = status_dev;
+  return launch_status(nvfp4::launch_gemm(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char* nvfp4_strerror(int status) {
   switch (status) {
     case NVFP4_OK: return "ok";

@@ -53,10 +53,26 @@ struct HistArgs {
   unsigned long long* hist;  // [3][nbins], accumulated into
 };
 
+struct GemmArgs {
+  const uint8_t* qa;    // M x K/2 codes (K contiguous)
+  const uint8_t* sfa;   // tiled scales of A (128 x 4 tiles of 512 bytes)
+  const float* alpha_a; // [1]
+  const uint8_t* qb;    // N x K/2 codes
+  const uint8_t* sfb;   // tiled scales of B
+  const float* alpha_b; // [1]
+  float* d;             // M x N, row stride ldd
+  int64_t M, N, K, ldd;
+  int* status;          // nullable
+};
+
 // TMA boxes of the bf16 input: 64 columns (128 bytes, the swizzle span) x 64 rows.
 constexpr int kBoxCols = 64;
 constexpr int kBoxRows = 64;
 cudaError_t make_tile_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t N, int64_t ld);
+// Packed FP4 codes (rows x row_bytes bytes, dense) read in 128-byte-swizzled
+// boxes of box_bytes x box_rows.
+cudaError_t make_codes_map(CUtensorMap* map, const uint8_t* q, int64_t rows, int64_t row_bytes, int box_bytes,
+                           int box_rows);
 
 // Grid of a persistent kernel on the current device: resident CTAs per SM
 // (at `threads` threads and `smem` bytes of dynamic shared memory, which the
@@ -91,5 +107,6 @@ cudaError_t launch_quant1d_46_max(const QuantArgs& a, bool row, bool col, bool s
 cudaError_t launch_quant2d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_error_hist(const HistArgs& a, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
 }  // namespace nvfp4

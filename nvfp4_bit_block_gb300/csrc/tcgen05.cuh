@@ -1,0 +1,102 @@
+// tcgen05.cuh -- fifth-generation tensor core (tcgen05) instructions of
+// sm_100a / sm_103a used by the NVFP4 GEMM, as inline PTX: tensor memory
+// (TMEM) allocation, block-scaled MMA with E2M1 operands and E4M3 scale
+// factors, shared-memory -> TMEM copies of the scale factors, completion
+// tracking on an mbarrier, and TMEM -> register loads for the epilogue.
+//
+// Shared-memory matrix descriptor (64 bits): start address >> 4 in bits 0-13,
+// leading-dimension byte offset >> 4 in bits 16-29, stride-dimension byte
+// offset >> 4 in bits 32-45, the descriptor version 1 in bits 46-47, base
+// offset 0 (tiles are 1024-byte aligned) and the layout (swizzle) type in
+// bits 61-63.
+//
+// Instruction descriptor of kind::mxf4nvf4 (32 bits): operand formats
+// (E2M1 = 1) in bits 7-9 (A) and 10-12 (B), both operands K-major (bits 15, 16
+// clear), N >> 3 in bits 17-22, scale type E4M3 (bit 23 clear), M >> 4 in
+// bits 24-28, scale-factor ids 0, dense K = 64 per instruction.
+#pragma once
+
+#include <cstdint>
+
+namespace nvfp4 {
+namespace tc5 {
+
+constexpr uint32_t kLayoutNone = 0;
+constexpr uint32_t kLayoutSwizzle128B = 2;
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)(layout & 7u) << 61);
+}
+
+constexpr uint32_t idesc_e2m1_e4m3(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Allocate `ncols` TMEM columns (a power of two, 32..512) for this CTA; the
+// whole warp executes it and the address is written to shared memory.
+__device__ __forceinline__ void alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void relinquish_alloc_permit() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before_thread_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_thread_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D (TMEM, fp32) (+)= A (smem) * B (smem)^T with one E4M3 scale per 16
+// E2M1 values along K for each row of A and of B (scale factors in TMEM).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// 32 rows x 16 bytes of shared memory (described by `src`) into 4 TMEM
+// columns of lanes 0-31, replicated to the four 32-lane quarters.
+__device__ __forceinline__ void cp_32x128b_warpx4(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
+}
+
+// The mbarrier at `bar` receives one arrival when every tcgen05 operation
+// this thread issued before has completed.
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Untiled bulk copy global -> shared, completion counted in bytes on `bar`
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+}  // namespace tc5
+}  // namespace nvfp4

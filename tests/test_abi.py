@@ -31,8 +31,8 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_functions() == ["nvfp4_amax", "nvfp4_dequantize", "nvfp4_error_histogram", "nvfp4_quantize",
-                                    "nvfp4_strerror"]
+    assert declared_functions() == ["nvfp4_amax", "nvfp4_dequantize", "nvfp4_error_histogram", "nvfp4_gemm",
+                                    "nvfp4_quantize", "nvfp4_strerror"]
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -128,6 +128,18 @@ def test_binding_raises_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nv, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         nv.lib()
+
+
+def test_gemm_rejects_bad_arguments(L):
+    g = L.nvfp4_gemm
+    ok = [ALIGNED, ALIGNED, ALIGNED2, ALIGNED, ALIGNED, ALIGNED2, 128, 128, 256, ALIGNED3, 128, None, None]
+    call = lambda changes: g(*[changes.get(i, v) for i, v in enumerate(ok)])
+    assert call({6: 100}) == -2 and call({7: 200}) == -2 and call({8: 128}) == -2   # M, N % 128; K % 256
+    assert call({8: 0}) == -2 and call({10: 64}) == -2                             # K = 0; ldd < N
+    assert call({6: 0}) == 0                                                       # empty: no-op
+    assert call({0: None}) == -1 and call({2: None}) == -1 and call({9: None}) == -1
+    assert call({0: ALIGNED + 8}) == -3 and call({1: ALIGNED + 4}) == -3           # codes, scales 16-byte
+    assert call({9: ALIGNED3 + 4}) == -3 and call({10: 130}) == -3                 # D 16-byte, ldd % 4
 
 
 def test_error_histogram_rejects_bad_arguments(L):
