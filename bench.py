@@ -24,7 +24,7 @@ bandwidth for the codec kernels, and for the stochastic-rounding kernels
 Philox calls per second against the SMs' wide-multiply rate.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-  python bench.py --report | --error-analysis | --once
+  python bench.py --report | --error-analysis | --once | --gemm
 
 Under torchrun (N > 1) every rank runs an independent replica (the path needs
 no exchange for independent tensors) and rank 0 prints the JSON line with the
@@ -579,6 +579,66 @@ def run_report(args):
         torch.cuda.empty_cache()
 
 
+def fp4_peak_tflops():
+    """Dense FP4 tensor peak: the measured bf16 GEMM peak x 6, the nominal
+    FP4 / BF16 ratio (13.5 / 2.25 PFLOP/s dense)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return 6.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 x 6 (nominal FP4/BF16 ratio)"
+    return 6.0 * 1900.0, "fallback bf16 x 6"
+
+
+def run_gemm(args):
+    """The linear layer's three NVFP4 GEMMs on the quantizer's own outputs
+    (tiled scales): fprop Y = X W (A = X rowwise, B = W columnwise), dgrad
+    dX = dY W^T (A = dY rowwise, B = W rowwise), wgrad dW = X^T dY (A = X
+    columnwise, B = dY columnwise).  One JSON line per GEMM: CUDA-event time
+    averaged over --steps launches after --warmup, TFLOP/s (2MNK) and the
+    fraction of the dense FP4 tensor peak."""
+    import torch
+
+    import nvfp4_bit_block_gb300 as nv
+
+    nv.lib()
+    q = {}
+    for p in parts_of("linear_layer"):
+        flags, sel = synthetic.workload_flags(p)
+        bits = synthetic.workload(p)
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+        del bits
+        am = nv.nvfp4_amax(x, flags, synthetic.RHT_SEED)
+        q[p] = nv.nvfp4_quantize(x, am, flags | nv.SF_SWIZZLED, sel, synthetic.SR_SEED, synthetic.RHT_SEED)
+        del x
+    torch.cuda.synchronize()
+    X, W, dY = (q[p] for p in parts_of("linear_layer"))
+    gemms = [("fprop Y = X W", X.q_row, X.s_row, X.alpha[0:1], W.q_col, W.s_col, W.alpha[1:2]),
+             ("dgrad dX = dY W^T", dY.q_row, dY.s_row, dY.alpha[0:1], W.q_row, W.s_row, W.alpha[0:1]),
+             ("wgrad dW = X^T dY", X.q_col, X.s_col, X.alpha[1:2], dY.q_col, dY.s_col, dY.alpha[1:2])]
+    peak, peak_kind = fp4_peak_tflops()
+    out_dtype = torch.bfloat16 if args.gemm_out == "bf16" else torch.float32
+    for name, qa, sa, aa, qb, sb, ab in gemms:
+        M, N, K = qa.shape[0], qb.shape[0], 2 * qa.shape[1]
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty((M, N), dtype=out_dtype, device="cuda")
+        for _ in range(max(3, args.warmup)):
+            nv.nvfp4_gemm(qa, sa, aa, qb, sb, ab, out=out, status=status)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            nv.nvfp4_gemm(qa, sa, aa, qb, sb, ab, out=out, status=status)
+        e1.record()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ms = e0.elapsed_time(e1) / args.steps
+        tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        print(json.dumps({"gemm": name, "M": M, "N": N, "K": K, "out": args.gemm_out, "ms": round(ms, 4),
+                          "TFLOP/s": round(tflops, 1),
+                          "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": round(peak, 1),
+                                       "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "peak_kind": peak_kind},
+                          "steps": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def run_error_analysis(args, nbins: int = 24):
     """Where the rounding error sits within the blocks of the workload's
     rowwise copy: standard NVFP4 (block max at 6, alpha over 6*448) against
@@ -711,6 +771,9 @@ def main():
                     help="print one JSON line per tensor, ablation and X-path size (2^20..2^30)")
     ap.add_argument("--error-analysis", action="store_true",
                     help="print the rowwise error histogram over the scaled value, standard vs 4/6")
+    ap.add_argument("--gemm", action="store_true",
+                    help="time the linear layer's three NVFP4 GEMMs (fprop, dgrad, wgrad) on the tensor cores")
+    ap.add_argument("--gemm-out", default="bf16", choices=["bf16", "fp32"], help="output type of --gemm")
     args = ap.parse_args()
     if args.workload in COMPOSITES and (args.flags is not None or args.sel is not None):
         ap.error("--flags / --sel apply to single-tensor workloads")
@@ -719,6 +782,9 @@ def main():
         return
     if args.once:
         run_once(args)
+        return
+    if args.gemm:
+        run_gemm(args)
         return
     if args.report:
         run_report(args)

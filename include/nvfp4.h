@@ -212,16 +212,18 @@ NVFP4_API int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int
  * scales per 16 values along K in the tiled 128 x 4 layout.  Each product is
  * formed from val(code) * e4m3(scale) per operand, the sum over K is
  * accumulated in fp32 by the tensor cores, and the result is multiplied by
- * alpha_a * alpha_b (rounded once to fp32) -- the dequantized operands'
- * product up to the order and rounding of the fp32 accumulation.
+ * alpha_a * alpha_b (rounded once to fp32, then to bf16 with out_is_bf16)
+ * -- the dequantized operands' product up to the order and rounding of the
+ * fp32 accumulation.
  *
  *   qa_dev       M x K/2 code bytes (16-byte aligned)
  *   sfa_dev      tiled scales of A: M/128 * K/64 blocks of 512 bytes
  *                (16-byte aligned)
  *   alpha_a_dev  one float (device): A's tensor scale (the alpha of its copy)
  *   qb_dev, sfb_dev, alpha_b_dev   the same for B (N rows)
- *   d_dev        fp32 M x N, row stride ldd elements (16-byte aligned,
- *                ldd % 4 == 0, ldd >= N)
+ *   out_is_bf16  0: D is fp32; 1: D is bf16 (round to nearest even)
+ *   d_dev        M x N, row stride ldd elements (16-byte aligned, ldd >= N,
+ *                ldd % 4 == 0 for fp32, ldd % 8 == 0 for bf16)
  *   status_dev   int (device) or NULL: set to NVFP4_ERR_PIPELINE if a tile
  *                copy or the tensor-core work did not complete within about
  *                a second (D is then incomplete); untouched on success
@@ -230,7 +232,8 @@ NVFP4_API int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int
  */
 NVFP4_API int nvfp4_gemm(const uint8_t* qa_dev, const uint8_t* sfa_dev, const float* alpha_a_dev,
                          const uint8_t* qb_dev, const uint8_t* sfb_dev, const float* alpha_b_dev, int64_t M,
-                         int64_t N, int64_t K, float* d_dev, int64_t ldd, int* status_dev, void* stream);
+                         int64_t N, int64_t K, int out_is_bf16, void* d_dev, int64_t ldd, int* status_dev,
+                         void* stream);
 
 /* Human-readable name of a status value (static string). */
 NVFP4_API const char* nvfp4_strerror(int status);

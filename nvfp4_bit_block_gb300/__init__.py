@@ -65,7 +65,8 @@ def lib() -> ctypes.CDLL:
                                             c.c_void_p, c.c_int, c.c_void_p, c.c_void_p]
         L.nvfp4_gemm.restype = c.c_int
         L.nvfp4_gemm.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
-                                 c.c_int64, c.c_int64, c.c_int64, c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p]
+                                 c.c_int64, c.c_int64, c.c_int64, c.c_int, c.c_void_p, c.c_int64, c.c_void_p,
+                                 c.c_void_p]
         L.nvfp4_strerror.restype = c.c_char_p
         L.nvfp4_strerror.argtypes = [c.c_int]
         _lib = L
@@ -215,11 +216,11 @@ def nvfp4_error_histogram(x, q_row, s_row, alpha, nbins: int = 24, out=None, str
     return out
 
 
-def nvfp4_gemm(qa, sfa, alpha_a, qb, sfb, alpha_b, out=None, status=None, stream=None):
-    """D (float32, M x N) = alpha_a * alpha_b * A * B^T: qa (M x K/2) / qb (N x K/2)
-    codes with K contiguous, sfa / sfb their scales in the tiled layout
-    (NVFP4_SF_SWIZZLED), alpha_a / alpha_b one-element device views of the
-    copies' alpha."""
+def nvfp4_gemm(qa, sfa, alpha_a, qb, sfb, alpha_b, out=None, out_dtype=None, status=None, stream=None):
+    """D (M x N, float32 or bfloat16) = alpha_a * alpha_b * A * B^T: qa (M x K/2) /
+    qb (N x K/2) codes with K contiguous, sfa / sfb their scales in the tiled
+    layout (NVFP4_SF_SWIZZLED), alpha_a / alpha_b one-element device views of
+    the copies' alpha."""
     import torch
     M, half = qa.shape
     N = qb.shape[0]
@@ -229,9 +230,12 @@ def nvfp4_gemm(qa, sfa, alpha_a, qb, sfb, alpha_b, out=None, status=None, stream
     if not qa.is_cuda:
         raise ValueError(f"qa must be a CUDA tensor (got {qa.device})")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+        out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=qa.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
     _on_device(qa.device, sfa=sfa, alpha_a=alpha_a, qb=qb, sfb=sfb, alpha_b=alpha_b, out=out, status=status)
+    bf16 = 1 if out.dtype == torch.bfloat16 else 0
     with torch.cuda.device(qa.device):
         _check(lib().nvfp4_gemm(_ptr(qa), _ptr(sfa), _ptr(alpha_a), _ptr(qb), _ptr(sfb), _ptr(alpha_b), M, N, K,
-                                _ptr(out), out.stride(0), _ptr(status), _stream_handle(stream)), "nvfp4_gemm")
+                                bf16, _ptr(out), out.stride(0), _ptr(status), _stream_handle(stream)), "nvfp4_gemm")
     return out

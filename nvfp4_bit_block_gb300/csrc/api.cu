@@ -156,15 +156,15 @@ int nvfp4_error_histogram(const void* x_dev, int64_t M, int64_t N, int64_t ld, c
 }
 
 int nvfp4_gemm(const uint8_t* qa_dev, const uint8_t* sfa_dev, const float* alpha_a_dev, const uint8_t* qb_dev,
-               const uint8_t* sfb_dev, const float* alpha_b_dev, int64_t M, int64_t N, int64_t K, float* d_dev,
-               int64_t ldd, int* status_dev, void* stream) {
+               const uint8_t* sfb_dev, const float* alpha_b_dev, int64_t M, int64_t N, int64_t K, int out_is_bf16,
+               void* d_dev, int64_t ldd, int* status_dev, void* stream) {
   if (M < 0 || N < 0 || K < 0 || M % 128 || N % 128 || K % 256 || ldd < N) return NVFP4_ERR_SHAPE;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_SHAPE;
   if (M == 0 || N == 0) return NVFP4_OK;
   if (K == 0) return NVFP4_ERR_SHAPE;
   if (!qa_dev || !sfa_dev || !alpha_a_dev || !qb_dev || !sfb_dev || !alpha_b_dev || !d_dev) return NVFP4_ERR_NULL;
   if (!aligned(qa_dev, 16) || !aligned(qb_dev, 16) || !aligned(sfa_dev, 16) || !aligned(sfb_dev, 16) ||
-      !aligned(d_dev, 16) || ldd % 4 || !aligned(alpha_a_dev, 4) || !aligned(alpha_b_dev, 4) ||
+      !aligned(d_dev, 16) || ldd % (out_is_bf16 ? 8 : 4) || !aligned(alpha_a_dev, 4) || !aligned(alpha_b_dev, 4) ||
       (status_dev && !aligned(status_dev, 4)))
     return NVFP4_ERR_ALIGN;
   nvfp4::GemmArgs a;
@@ -179,6 +179,7 @@ int nvfp4_gemm(const uint8_t* qa_dev, const uint8_t* sfa_dev, const float* alpha
   a.N = N;
   a.K = K;
   a.ldd = ldd;
+  a.out_bf16 = out_is_bf16 ? 1 : 0;
   a.status = status_dev;
   return launch_status(nvfp4::launch_gemm(a, static_cast<cudaStream_t>(stream)));
 }

@@ -1,26 +1,31 @@
 // gemm.cu -- NVFP4 block-scaled GEMM on the fifth-generation tensor cores.
 //
-// D = alpha_a * alpha_b * (A * B^T), fp32 out: A (M x K) and B (N x K) are
-// NVFP4 operands exactly as nvfp4_quantize writes them with
+// D = alpha_a * alpha_b * (A * B^T), fp32 or bf16 out: A (M x K) and B (N x K)
+// are NVFP4 operands exactly as nvfp4_quantize writes them with
 // NVFP4_SF_SWIZZLED -- packed E2M1 codes, K contiguous (a rowwise copy, or a
 // columnwise copy for a transposed operand), and E4M3 scales per 16 values
 // along K in the tiled 128 x 4 layout -- so the quantizer's outputs feed the
 // tensor cores without a re-layout ("NVFP4 revolutionizes AI training"
 // headline page: Blackwell multiplies FP4 matrices natively).
 //
-// One CTA computes a 128 x 128 tile of D over all of K.  Four warps:
-//   - warp 0 allocates 256 TMEM columns; its lane 0 is the producer: per
+// Persistent CTAs (one per SM) walk the 128 x 128 output tiles, N fastest
+// (the CTAs in flight share an A band, B stays in L2).  Six warps:
+//   - warp 0 allocates 512 TMEM columns; its lane 0 is the producer: per
 //     K step of 256 values it loads a 128 x 128-byte tile of A and of B with
 //     TMA (128-byte swizzle, the K-major layout the MMA reads) and the two
-//     2 KB scale blocks with bulk copies, into one of four shared-memory
+//     2 KB scale blocks with bulk copies, into one of six shared-memory
 //     stages, completion on the stage's "full" mbarrier;
-//   - warp 1 lane 0 issues, per stage, four scale copies to TMEM and four
-//     tcgen05.mma (kind::mxf4nvf4, M = 128, N = 128, K = 64, fp32 accumulator
-//     in TMEM columns 0-127), then a commit that frees the stage;
-//   - all four warps then read the accumulator (one TMEM lane quarter each),
-//     apply alpha_a * alpha_b and store D.
+//   - warp 1 lane 0 issues, per stage, the scale copies to TMEM and four
+//     tcgen05.mma (kind::mxf4nvf4, M = 128, N = 128, K = 64) into one of two
+//     fp32 accumulators in TMEM (columns 0-127, 128-255), then a commit that
+//     frees the stage; after a tile's last K step a commit hands the
+//     accumulator to the epilogue;
+//   - warps 2-5 (one TMEM lane quarter each) read an accumulator, release it
+//     to the MMA warp, apply alpha_a * alpha_b and store D, while the MMA warp
+//     fills the other accumulator.
 // Every wait is bounded (about a second); a wait that runs out writes
-// NVFP4_ERR_PIPELINE to the status word, and TMEM is released on every path.
+// NVFP4_ERR_PIPELINE to the status word, the loops stop, the tensor-core work
+// already issued is drained, and TMEM is released on every path.
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 #include "tcgen05.cuh"
@@ -31,18 +36,25 @@ namespace {
 
 constexpr int kBM = 128, kBN = 128;
 constexpr int kBK = 256;                         // FP4 values per K step (128 bytes of codes per row)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kTileA = kBM * kBK / 2;            // 16 KB
 constexpr int kTileB = kBN * kBK / 2;            // 16 KB
 constexpr int kSfBlock = 512;                    // scales of 128 rows x 64 values
 constexpr int kSfBytes = (kBK / 64) * kSfBlock;  // 2 KB per operand and stage
 constexpr int kStageBytes = kTileA + kTileB + 2 * kSfBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers, TMEM address */ + 1024 /* alignment */;
-constexpr uint32_t kTmemCols = 256;              // accumulator 0-127, scale factors 128-255
-constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 512;              // accumulators 0-255, scale factors 256-447
+constexpr uint32_t kSfCol0 = 256;
+constexpr int kThreads = 192;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -51,19 +63,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 1024-byte alignment for the 128-byte swizzle
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages), done = smem_u32(bars + 2 * kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t accf0 = smem_u32(bars + 2 * kStages), acce0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  int* abort_flag = reinterpret_cast<int*>(bars + 2 * kStages + 6);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t m0 = (int64_t)blockIdx.y * kBM, n0 = (int64_t)blockIdx.x * kBN;
   const int nk = (int)(a.K / kBK);
+  const int64_t tiles_n = a.N / kBN, tiles = (a.M / kBM) * tiles_n;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       tma::mbar_init(full0 + 8 * s, 1);
       tma::mbar_init(empty0 + 8 * s, 1);
     }
-    tma::mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      tma::mbar_init(accf0 + 8 * b, 1);
+      tma::mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
+    }
+    tma::mbar_init(drain, 1);
+    *abort_flag = 0;
     tma::fence_barrier_init();
   }
   if (warp == 0) {
@@ -74,85 +94,135 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc5::fence_after_thread_sync();
   const uint32_t tmem = *tmem_slot;
+  volatile int* abort_v = abort_flag;
 
-  bool ok = true;
-  if (warp == 0 && lane == 0) {
-    // producer: TMA tiles of A and B, bulk copies of their scale blocks
-    const int64_t sf_tiles_k = a.K / 64;  // 512-byte scale blocks per 128-row band
-    const uint8_t* sfa = a.sfa + (blockIdx.y * sf_tiles_k) * kSfBlock;
-    const uint8_t* sfb = a.sfb + (blockIdx.x * sf_tiles_k) * kSfBlock;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-      if (kb >= kStages && !tma::wait(empty0 + 8 * s, ph ^ 1u)) {
-        ok = false;
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer: TMA tiles of A and B, bulk copies of their scale blocks
+      const int64_t sf_tiles_k = a.K / 64;  // 512-byte scale blocks per 128-row band
+      int64_t g = 0;                        // K steps issued by this CTA
+      for (int64_t t = blockIdx.x; t < tiles && !*abort_v; t += gridDim.x) {
+        const int64_t tm = t / tiles_n, tn = t - tm * tiles_n;
+        const uint8_t* sfa = a.sfa + tm * sf_tiles_k * kSfBlock;
+        const uint8_t* sfb = a.sfb + tn * sf_tiles_k * kSfBlock;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = (int)(g % kStages);
+          const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+          if (g >= kStages && !tma::wait(empty0 + 8 * s, ph ^ 1u)) {
+            *abort_v = 1;
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          const uint32_t full = full0 + 8 * s;
+          tma::arrive_expect_tx(full, kStageBytes);
+          tma::load_2d(smem_u32(st), &amap, kb * (kBK / 2), (int)(tm * kBM), full);
+          tma::load_2d(smem_u32(st + kTileA), &bmap, kb * (kBK / 2), (int)(tn * kBN), full);
+          tc5::bulk_g2s(smem_u32(st + kTileA + kTileB), sfa + (int64_t)kb * kSfBytes, kSfBytes, full);
+          tc5::bulk_g2s(smem_u32(st + kTileA + kTileB + kSfBytes), sfb + (int64_t)kb * kSfBytes, kSfBytes, full);
+        }
       }
-      uint8_t* st = smem + s * kStageBytes;
-      const uint32_t full = full0 + 8 * s;
-      tma::arrive_expect_tx(full, kStageBytes);
-      tma::load_2d(smem_u32(st), &amap, kb * (kBK / 2), (int)m0, full);
-      tma::load_2d(smem_u32(st + kTileA), &bmap, kb * (kBK / 2), (int)n0, full);
-      tc5::bulk_g2s(smem_u32(st + kTileA + kTileB), sfa + (int64_t)kb * kSfBytes, kSfBytes, full);
-      tc5::bulk_g2s(smem_u32(st + kTileA + kTileB + kSfBytes), sfb + (int64_t)kb * kSfBytes, kSfBytes, full);
     }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer
-    constexpr uint32_t idesc = tc5::idesc_e2m1_e4m3(kBM, kBN);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-      if (!tma::wait(full0 + 8 * s, ph)) {
-        ok = false;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer
+      constexpr uint32_t idesc = tc5::idesc_e2m1_e4m3(kBM, kBN);
+      int64_t g = 0;
+      int li = 0;  // tiles of this CTA
+      for (int64_t t = blockIdx.x; t < tiles && !*abort_v; t += gridDim.x, ++li) {
+        const int ab = li & 1;
+        const uint32_t acc = tmem + (uint32_t)(ab * kBN);
+        if (li >= 2 && !tma::wait(acce0 + 8 * ab, (uint32_t)((li >> 1) & 1) ^ 1u)) {
+          *abort_v = 1;
+          break;
+        }
+        tc5::fence_after_thread_sync();
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = (int)(g % kStages);
+          const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+          if (!tma::wait(full0 + 8 * s, ph)) {
+            *abort_v = 1;
+            break;
+          }
+          tc5::fence_after_thread_sync();
+          const uint8_t* st = smem + s * kStageBytes;
+          const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kTileA);
+          const uint32_t sfa_base = smem_u32(st + kTileA + kTileB), sfb_base = sfa_base + kSfBytes;
+#pragma unroll
+          for (int j = 0; j < kBK / 64; ++j) {
+            const uint32_t sfa_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 4 * j);
+            const uint32_t sfb_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 16 + 4 * j);
+            tc5::cp_32x128b_warpx4(sfa_t, tc5::smem_desc(sfa_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
+            tc5::cp_32x128b_warpx4(sfb_t, tc5::smem_desc(sfb_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
+            // K step j: 64 values = 32 bytes into each 128-byte swizzled row
+            const uint64_t adesc = tc5::smem_desc(a_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
+            const uint64_t bdesc = tc5::smem_desc(b_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
+            tc5::mma_nvf4(acc, adesc, bdesc, idesc, sfa_t, sfb_t, kb > 0 || j > 0);
+          }
+          tc5::commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
+        }
+        if (*abort_v) break;
+        tc5::commit(accf0 + 8 * ab);  // the accumulator is complete once these MMAs are
+      }
+      tc5::commit(drain);  // arrives when every MMA issued above has completed
+    }
+  } else {
+    // epilogue: warp w reads TMEM lane quarter w % 4 = rows 32 * (w % 4) + lane of the tile
+    const int q = warp & 3;
+    const float scale = __fmul_rn(a.alpha_a[0], a.alpha_b[0]);
+    int li = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++li) {
+      const int ab = li & 1;
+      const bool ready = tma::wait(accf0 + 8 * ab, (uint32_t)((li >> 1) & 1));
+      if (!__all_sync(0xFFFFFFFFu, ready) || *abort_v) {
+        if (lane == 0) *abort_v = 1;
         break;
       }
       tc5::fence_after_thread_sync();
-      const uint8_t* st = smem + s * kStageBytes;
-      const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kTileA);
-      const uint32_t sfa_base = smem_u32(st + kTileA + kTileB), sfb_base = sfa_base + kSfBytes;
-#pragma unroll
-      for (int j = 0; j < kBK / 64; ++j) {
-        const uint32_t sfa_t = tmem + 128u + (uint32_t)(s * 32 + 4 * j);
-        const uint32_t sfb_t = tmem + 128u + (uint32_t)(s * 32 + 16 + 4 * j);
-        tc5::cp_32x128b_warpx4(sfa_t, tc5::smem_desc(sfa_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
-        tc5::cp_32x128b_warpx4(sfb_t, tc5::smem_desc(sfb_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
-        // K step j: 64 values = 32 bytes into each 128-byte swizzled row
-        const uint64_t adesc = tc5::smem_desc(a_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
-        const uint64_t bdesc = tc5::smem_desc(b_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
-        tc5::mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t, sfb_t, kb > 0 || j > 0);
-      }
-      tc5::commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
-    }
-    tc5::commit(done);  // arrives when every MMA issued above has completed
-  }
-  __syncwarp();
-  if (!ok && a.status) atomicExch(a.status, kStatusPipeline);
-
-  // epilogue: lane quarter `warp` of the accumulator = rows m0 + 32*warp + lane
-  const bool finished = tma::wait(done, 0);
-  __syncwarp();
-  tc5::fence_after_thread_sync();
-  if (finished) {
-    const float scale = __fmul_rn(a.alpha_a[0], a.alpha_b[0]);
-    float* drow = a.d + (m0 + 32 * warp + lane) * a.ldd + n0;
+      const int64_t tm = t / tiles_n, tn = t - tm * tiles_n;
+      const int64_t row = tm * kBM + 32 * q + lane;
+      const uint32_t acc = tmem + (uint32_t)(ab * kBN) + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t r[32];
-      tc5::ld_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), r);
-      tc5::wait_ld();
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tc5::ld_32x32b_x32(acc + (uint32_t)(32 * c), r);
+        tc5::wait_ld();
+        if (c == kBN / 32 - 1) {  // the accumulator is in registers: hand it back
+          tc5::fence_before_thread_sync();
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8 * ab) : "memory");
+        }
+        const int64_t col = tn * kBN + 32 * c;
+        if (a.out_bf16) {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(a.d) + row * a.ldd + col;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v;
-        v.x = __fmul_rn(__uint_as_float(r[4 * q + 0]), scale);
-        v.y = __fmul_rn(__uint_as_float(r[4 * q + 1]), scale);
-        v.z = __fmul_rn(__uint_as_float(r[4 * q + 2]), scale);
-        v.w = __fmul_rn(__uint_as_float(r[4 * q + 3]), scale);
-        *reinterpret_cast<float4*>(drow + 32 * c + 4 * q) = v;
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * v + 0]), scale), __fmul_rn(__uint_as_float(r[8 * v + 1]), scale));
+            w.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * v + 2]), scale), __fmul_rn(__uint_as_float(r[8 * v + 3]), scale));
+            w.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * v + 4]), scale), __fmul_rn(__uint_as_float(r[8 * v + 5]), scale));
+            w.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * v + 6]), scale), __fmul_rn(__uint_as_float(r[8 * v + 7]), scale));
+            *reinterpret_cast<uint4*>(dst + 8 * v) = w;
+          }
+        } else {
+          float* dst = reinterpret_cast<float*>(a.d) + row * a.ldd + col;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 f;
+            f.x = __fmul_rn(__uint_as_float(r[4 * v + 0]), scale);
+            f.y = __fmul_rn(__uint_as_float(r[4 * v + 1]), scale);
+            f.z = __fmul_rn(__uint_as_float(r[4 * v + 2]), scale);
+            f.w = __fmul_rn(__uint_as_float(r[4 * v + 3]), scale);
+            *reinterpret_cast<float4*>(dst + 4 * v) = f;
+          }
+        }
       }
     }
-  } else if (lane == 0 && a.status) {
-    atomicExch(a.status, kStatusPipeline);
   }
+  __syncwarp();
+  __syncthreads();
+  // drain the tensor-core work issued by the MMA thread (its last commit), then free TMEM
+  const bool drained = tma::wait(drain, 0);
+  if (tid == 0 && (*abort_v || !drained) && a.status) atomicExch(a.status, kStatusPipeline);
   tc5::fence_before_thread_sync();
   __syncthreads();
   if (warp == 0) tc5::dealloc(tmem, kTmemCols);
@@ -161,22 +231,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  static std::atomic<int> configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
-  }
+  static std::atomic<int> grid_cap[64] = {};
+  int cap = 0;
+  const cudaError_t ge = resident_grid(gemm_nvf4_kernel, kThreads, kSmemBytes, grid_cap, cap);
+  if (ge != cudaSuccess) return ge;
   CUtensorMap amap, bmap;
-  e = make_codes_map(&amap, a.qa, a.M, a.K / 2, kBK / 2, kBM);
+  cudaError_t e = make_codes_map(&amap, a.qa, a.M, a.K / 2, kBK / 2, kBM);
   if (e != cudaSuccess) return e;
   e = make_codes_map(&bmap, a.qb, a.N, a.K / 2, kBK / 2, kBN);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(a.N / kBN), (unsigned)(a.M / kBM), 1);
-  gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, amap, bmap);
+  const int64_t tiles = (a.M / kBM) * (a.N / kBN);
+  const int64_t grid = tiles < cap ? tiles : cap;
+  gemm_nvf4_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, amap, bmap);
   return cudaGetLastError();
 }
 

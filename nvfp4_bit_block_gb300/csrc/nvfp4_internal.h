@@ -60,8 +60,9 @@ struct GemmArgs {
   const uint8_t* qb;    // N x K/2 codes
   const uint8_t* sfb;   // tiled scales of B
   const float* alpha_b; // [1]
-  float* d;             // M x N, row stride ldd
+  void* d;              // M x N, row stride ldd elements
   int64_t M, N, K, ldd;
+  int out_bf16;         // D in bf16 (else fp32)
   int* status;          // nullable
 };
 

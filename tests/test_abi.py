@@ -132,14 +132,17 @@ def test_binding_raises_without_the_library(monkeypatch, tmp_path):
 
 def test_gemm_rejects_bad_arguments(L):
     g = L.nvfp4_gemm
-    ok = [ALIGNED, ALIGNED, ALIGNED2, ALIGNED, ALIGNED, ALIGNED2, 128, 128, 256, ALIGNED3, 128, None, None]
+    g.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                                                                  ctypes.c_void_p, ctypes.c_void_p]
+    ok = [ALIGNED, ALIGNED, ALIGNED2, ALIGNED, ALIGNED, ALIGNED2, 128, 128, 256, 0, ALIGNED3, 128, None, None]
     call = lambda changes: g(*[changes.get(i, v) for i, v in enumerate(ok)])
     assert call({6: 100}) == -2 and call({7: 200}) == -2 and call({8: 128}) == -2   # M, N % 128; K % 256
-    assert call({8: 0}) == -2 and call({10: 64}) == -2                             # K = 0; ldd < N
+    assert call({8: 0}) == -2 and call({11: 64}) == -2                             # K = 0; ldd < N
     assert call({6: 0}) == 0                                                       # empty: no-op
-    assert call({0: None}) == -1 and call({2: None}) == -1 and call({9: None}) == -1
+    assert call({0: None}) == -1 and call({2: None}) == -1 and call({10: None}) == -1
     assert call({0: ALIGNED + 8}) == -3 and call({1: ALIGNED + 4}) == -3           # codes, scales 16-byte
-    assert call({9: ALIGNED3 + 4}) == -3 and call({10: 130}) == -3                 # D 16-byte, ldd % 4
+    assert call({10: ALIGNED3 + 4}) == -3 and call({11: 130}) == -3                # D 16-byte, ldd % 4
+    assert call({9: 1, 11: 132}) == -3                                             # bf16 rows: ldd % 8
 
 
 def test_error_histogram_rejects_bad_arguments(L):
