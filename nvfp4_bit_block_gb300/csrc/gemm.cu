@@ -8,18 +8,22 @@
 // tensor cores without a re-layout ("NVFP4 revolutionizes AI training"
 // headline page: Blackwell multiplies FP4 matrices natively).
 //
-// Persistent CTAs (one per SM) walk the 128 x 128 output tiles, N fastest
-// (the CTAs in flight share an A band, B stays in L2).  Six warps:
+// Persistent CTAs (one per SM) walk the 128 x 128 output tiles in groups of
+// eight M tiles (see tile_coords), so that the CTAs in flight share A and B
+// tiles in L2.  Six warps:
 //   - warp 0 allocates 512 TMEM columns; its lane 0 is the producer: per
 //     K step of 256 values it loads a 128 x 128-byte tile of A and of B with
 //     TMA (128-byte swizzle, the K-major layout the MMA reads) and the two
 //     2 KB scale blocks with bulk copies, into one of six shared-memory
 //     stages, completion on the stage's "full" mbarrier;
-//   - warp 1 lane 0 issues, per stage, the scale copies to TMEM and four
-//     tcgen05.mma (kind::mxf4nvf4, M = 128, N = 128, K = 64) into one of two
-//     fp32 accumulators in TMEM (columns 0-127, 128-255), then a commit that
-//     frees the stage; after a tile's last K step a commit hands the
-//     accumulator to the epilogue;
+//   - warps 6-9 (one TMEM lane quarter each) move each stage's scale blocks
+//     from shared memory to TMEM (tcgen05.st; 16 bytes per lane = the 4 scale
+//     bytes of rows l, l+32, l+64, l+96, in every lane quarter), off the MMA
+//     warp's in-order path, and signal the stage's "scales" mbarrier;
+//   - warp 1 lane 0 issues, per stage, four tcgen05.mma (kind::mxf4nvf4,
+//     M = 128, N = 128, K = 64) into one of two fp32 accumulators in TMEM
+//     (columns 0-127, 128-255), then a commit that frees the stage; after a
+//     tile's last K step a commit hands the accumulator to the epilogue;
 //   - warps 2-5 (one TMEM lane quarter each) read an accumulator, release it
 //     to the MMA warp, apply alpha_a * alpha_b and store D, while the MMA warp
 //     fills the other accumulator.
@@ -45,10 +49,28 @@ constexpr int kStageBytes = kTileA + kTileB + 2 * kSfBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers, TMEM address */ + 1024 /* alignment */;
 constexpr uint32_t kTmemCols = 512;              // accumulators 0-255, scale factors 256-447
 constexpr uint32_t kSfCol0 = 256;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSfWarp0 = 6;  // warps 6-9 move the scale blocks to TMEM
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Tile t -> (M tile, N tile), grouped: kGroupM consecutive M tiles are walked
+// N tile by N tile, so the CTAs in flight cover a block of about kGroupM x
+// (SMs / kGroupM) tiles and each A and B tile is shared by several of them.
+#ifndef NVFP4_GEMM_GROUP_M
+#define NVFP4_GEMM_GROUP_M 8
+#endif
+constexpr int64_t kGroupM = NVFP4_GEMM_GROUP_M;
+
+__device__ __forceinline__ void tile_coords(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t& tm, int64_t& tn) {
+  const int64_t per_group = kGroupM * tiles_n;
+  const int64_t g = t / per_group, r = t - g * per_group;
+  const int64_t m0 = g * kGroupM;
+  const int64_t gm = (tiles_m - m0) < kGroupM ? (tiles_m - m0) : kGroupM;  // M tiles in this (last) group
+  tm = m0 + r % gm;
+  tn = r / gm;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -68,10 +90,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   int* abort_flag = reinterpret_cast<int*>(bars + 2 * kStages + 6);
+  const uint32_t sfr0 = smem_u32(bars + 2 * kStages + 7);  // per stage: scales in TMEM
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nk = (int)(a.K / kBK);
-  const int64_t tiles_n = a.N / kBN, tiles = (a.M / kBM) * tiles_n;
+  const int64_t tiles_n = a.N / kBN, tiles_m = a.M / kBM, tiles = tiles_m * tiles_n;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -83,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma::mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
     }
     tma::mbar_init(drain, 1);
+    for (int st = 0; st < kStages; ++st) tma::mbar_init(sfr0 + 8 * st, 4);  // one arrival per scale warp
     *abort_flag = 0;
     tma::fence_barrier_init();
   }
@@ -102,7 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t sf_tiles_k = a.K / 64;  // 512-byte scale blocks per 128-row band
       int64_t g = 0;                        // K steps issued by this CTA
       for (int64_t t = blockIdx.x; t < tiles && !*abort_v; t += gridDim.x) {
-        const int64_t tm = t / tiles_n, tn = t - tm * tiles_n;
+        int64_t tm, tn;
+        tile_coords(t, tiles_m, tiles_n, tm, tn);
         const uint8_t* sfa = a.sfa + tm * sf_tiles_k * kSfBlock;
         const uint8_t* sfb = a.sfb + tn * sf_tiles_k * kSfBlock;
         for (int kb = 0; kb < nk; ++kb, ++g) {
@@ -139,20 +164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = (int)(g % kStages);
           const uint32_t ph = (uint32_t)(g / kStages) & 1u;
-          if (!tma::wait(full0 + 8 * s, ph)) {
+          // the tiles have arrived and the scale warps have put the stage's scales in TMEM
+          if (!tma::wait(full0 + 8 * s, ph) || !tma::wait(sfr0 + 8 * s, ph)) {
             *abort_v = 1;
             break;
           }
           tc5::fence_after_thread_sync();
           const uint8_t* st = smem + s * kStageBytes;
           const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kTileA);
-          const uint32_t sfa_base = smem_u32(st + kTileA + kTileB), sfb_base = sfa_base + kSfBytes;
 #pragma unroll
           for (int j = 0; j < kBK / 64; ++j) {
             const uint32_t sfa_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 4 * j);
             const uint32_t sfb_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 16 + 4 * j);
-            tc5::cp_32x128b_warpx4(sfa_t, tc5::smem_desc(sfa_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
-            tc5::cp_32x128b_warpx4(sfb_t, tc5::smem_desc(sfb_base + j * kSfBlock, 0, 128, tc5::kLayoutNone));
             // K step j: 64 values = 32 bytes into each 128-byte swizzled row
             const uint64_t adesc = tc5::smem_desc(a_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
             const uint64_t bdesc = tc5::smem_desc(b_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
@@ -165,6 +188,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc5::commit(drain);  // arrives when every MMA issued above has completed
     }
+  } else if (warp >= kSfWarp0) {
+    // scale warps: warp w writes TMEM lane quarter w % 4; every quarter gets the
+    // same 16 bytes per lane (the four row groups of the 128 x 4 scale tile)
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    int64_t g = 0;
+    bool stop = false;  // warp-uniform: every lane takes the same path to the .sync.aligned stores
+    for (int64_t t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+      stop = __any_sync(0xFFFFFFFFu, *abort_v != 0);
+      for (int kb = 0; kb < nk && !stop; ++kb, ++g) {
+        const int s = (int)(g % kStages);
+        const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+        const bool arrived = tma::wait(full0 + 8 * s, ph);
+        if (!__all_sync(0xFFFFFFFFu, arrived)) {
+          if (lane == 0) *abort_v = 1;
+          stop = true;
+          break;
+        }
+        const uint8_t* sf = smem + s * kStageBytes + kTileA + kTileB;
+#pragma unroll
+        for (int j = 0; j < kBK / 64; ++j) {
+          const uint4 va = *reinterpret_cast<const uint4*>(sf + j * kSfBlock + 16 * lane);
+          const uint4 vb = *reinterpret_cast<const uint4*>(sf + kSfBytes + j * kSfBlock + 16 * lane);
+          tc5::st_32x32b_x4(tmem + lane_base + kSfCol0 + (uint32_t)(s * 32 + 4 * j), va);
+          tc5::st_32x32b_x4(tmem + lane_base + kSfCol0 + (uint32_t)(s * 32 + 16 + 4 * j), vb);
+        }
+        tc5::wait_st();
+        tc5::fence_before_thread_sync();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sfr0 + 8 * s) : "memory");
+      }
+    }
   } else {
     // epilogue: warp w reads TMEM lane quarter w % 4 = rows 32 * (w % 4) + lane of the tile
     const int q = warp & 3;
@@ -173,12 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++li) {
       const int ab = li & 1;
       const bool ready = tma::wait(accf0 + 8 * ab, (uint32_t)((li >> 1) & 1));
-      if (!__all_sync(0xFFFFFFFFu, ready) || *abort_v) {
+      // warp-uniform decision before the .sync.aligned TMEM loads
+      if (!__all_sync(0xFFFFFFFFu, ready) || __any_sync(0xFFFFFFFFu, *abort_v != 0)) {
         if (lane == 0) *abort_v = 1;
         break;
       }
       tc5::fence_after_thread_sync();
-      const int64_t tm = t / tiles_n, tn = t - tm * tiles_n;
+      int64_t tm, tn;
+      tile_coords(t, tiles_m, tiles_n, tm, tn);
       const int64_t row = tm * kBM + 32 * q + lane;
       const uint32_t acc = tmem + (uint32_t)(ab * kBN) + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1

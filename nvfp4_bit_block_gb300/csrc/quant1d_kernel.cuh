@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
     if (COL && cp_ok) {
       const int p = cp_p;
-#pragma unroll 1
+#pragma unroll
       for (int k = 0; k < 2; ++k) {  // row block rb of column pair p (both columns)
         const int rb = cp_rb0 + 2 * k;
         if (16 * rb >= rows) break;

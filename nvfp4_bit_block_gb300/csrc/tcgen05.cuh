@@ -90,6 +90,15 @@ __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 4 consecutive 32-bit TMEM columns of this thread's lane (the warp's lane
+// quarter is in the address), then the wait for the warp's stores.
+__device__ __forceinline__ void st_32x32b_x4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Untiled bulk copy global -> shared, completion counted in bytes on `bar`
 // (both addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
