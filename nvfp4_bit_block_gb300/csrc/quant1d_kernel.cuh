@@ -217,12 +217,23 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
 
   const int64_t M = a.M, N = a.N;
   const int tid = threadIdx.x;
-  if ((tid & 127) != 127) tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);
+  auto issue = [&](int b, const tile::Coord& c) {
+    const uint32_t bar = b ? bar1 : bar0;
+    tma::arrive_expect_tx(bar, tile::kTileBytes);
+    if (NOCOPY) return;
+    const uint32_t dst = tile::smem_u32(bufs + b * tile::kTileBytes);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
+  };
+  tile::Walker w;
+  w.init(M, N);
   if (tid == 0) {
     tma::mbar_init(bar0, 1);
     tma::mbar_init(bar1, 1);
     tma::fence_barrier_init();
+    if (w.valid()) issue(0, w.coord());  // the first tile is in flight while the tables are built
   }
+  if ((tid & 127) != 127) tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);
   __syncthreads();  // barriers and tables ready
   const CopyScales scR = make_scales(alpha_r, tbl);
   const CopyScales scC = make_scales(alpha_c, tbl + 128);
@@ -245,18 +256,6 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
   const uint32_t c_base = (cp_p >> 5) * 8192 + (cp_p & 3) * 4;
   const uint32_t c_chunk = (uint32_t)((cp_p & 31) >> 2) << 4;
 
-  auto issue = [&](int b, const tile::Coord& c) {
-    const uint32_t bar = b ? bar1 : bar0;
-    tma::arrive_expect_tx(bar, tile::kTileBytes);
-    if (NOCOPY) return;
-    const uint32_t dst = tile::smem_u32(bufs + b * tile::kTileBytes);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
-  };
-
-  tile::Walker w;
-  w.init(M, N);
-  if (tid == 0 && w.valid()) issue(0, w.coord());
   for (int it = 0; w.valid(); w = w.next(), ++it) {
     const int b = kDB ? (it & 1) : 0;
     uint8_t* buf = bufs + b * tile::kTileBytes;
@@ -361,7 +360,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
     if (COL && cp_ok) {
       const int p = cp_p;
-#pragma unroll
+      // both tasks in flight at once, except with SR (its register budget is spent on Philox)
+      constexpr int kColUnroll = SR ? 1 : 2;
+#pragma unroll kColUnroll
       for (int k = 0; k < 2; ++k) {  // row block rb of column pair p (both columns)
         const int rb = cp_rb0 + 2 * k;
         if (16 * rb >= rows) break;
