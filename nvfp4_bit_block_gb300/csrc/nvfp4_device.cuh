@@ -203,23 +203,23 @@ __device__ __forceinline__ uint32_t rht_sign_bits(uint32_t k0, uint32_t k1) {
 // ---------------------------------------------------------------- rounding
 // Stochastic rounding of v onto the E2M1 grid with block maximum Q: with
 // m = min(|v|, Q) between grid neighbours lo <= m < hi, return hi iff
-// (w >> 8) * 2^-24 < (m - lo) / (hi - lo); the sign of v is kept.  All steps
-// are exact (power-of-two step sizes).  The step hi - lo is 2^(e-1) for m in
-// [2^e, 2^(e+1)), e = 0, 1, 2, and 0.5 below 1: both it and its reciprocal
-// are formed on the exponent field (the step is max(2^e, 1) / 2; the
-// reciprocal's biased exponent is 254 minus the step's).
+// u = (w >> 8) * 2^-24 < p = (m - lo) / (hi - lo); the sign of v is kept.
+// The step hi - lo is 2^(e-1) for m in [2^e, 2^(e+1)), e = 0, 1, 2, and 1/2
+// below 1 (max(2^e, 1) / 2, formed on the exponent field, as is its
+// reciprocal).  In units of the step m is t = f + p with f = floor(t) the
+// grid point lo, and hi is chosen exactly when t - u > f; since u lies in
+// [0, 1), t - u lies in (f, f + 1) when u < p and in (f - 1, f] otherwise,
+// so the grid point is q = ceil(t - u).  t - u is formed by one fused
+// multiply-add rounded upward: that rounding never passes an integer (the
+// integers up to 4 are floats), so ceil sees the exact decision.
 __device__ __forceinline__ float sr_round(float v, float Q, uint32_t w) {
   const float m = fminf(fabsf(v), Q);
-  const uint32_t sb = max(__float_as_uint(m) & 0x7F800000u, 0x3F800000u) - 0x00800000u;
-  const float step = __uint_as_float(sb);
-  const float rstep = __uint_as_float(0x7F000000u - sb);
-  // in units of the step: m / step = t, lo = f * step with f = floor(t), and
-  // the fraction p = t - f (every product and difference here is exact)
-  const float t = __fmul_rn(m, rstep);
-  const float f = floorf(t);
-  const float p = __fsub_rn(t, f);
-  const float u = __fmul_rn((float)(w >> 8), 0x1p-24f);
-  const float g = __fmul_rn((u < p) ? __fadd_rn(f, 1.0f) : f, step);
+  const int sb = max((int)(__float_as_uint(m) & 0x7F800000u) - 0x00800000, 0x3F000000);
+  const float step = __int_as_float(sb);
+  const float rstep = __int_as_float(0x7F000000 - sb);
+  const float t = __fmul_rn(m, rstep);  // exact: a power-of-two scaling
+  const float d = __fmaf_ru(__uint2float_rn(w >> 8), -0x1p-24f, t);
+  const float g = __fmul_rn(ceilf(d), step);
   return copysignf(g, v);
 }
 

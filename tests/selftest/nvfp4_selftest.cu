@@ -24,7 +24,8 @@
 // RHT sign word) with cuRAND's device implementation of the same generator,
 // an independent one, over pseudo-random and extreme counters and keys.  A
 // fourth launches the 1D quantize kernel in a variant that arms its tile
-// barriers but issues no copy, so that the bounded wait runs out.
+// barriers but issues no copy, so that the bounded wait runs out.  A fifth
+// runs the kernels' stochastic rounding alone on given values and words.
 #include <cstdint>
 
 #include <curand_philox4x32_x.h>
@@ -274,6 +275,37 @@ NVFP4_API int nvfp4_test_quantize_no_copy(const void* x_dev, int64_t M, int64_t 
   const cudaError_t e =
       nvfp4::q1d::launch<true, true, false, false, nvfp4::kSelMAE, 0, true>(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// The kernels' stochastic rounding alone: out[i] = sr_round(v[i], Q, w[i]).
+__global__ void sr_round_kernel(const float* v, const uint32_t* w, int64_t n, float Q, float* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = sr_round(v[i], Q, w[i]);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+// Test hook: run the kernels' stochastic rounding onto the E2M1 grid (block
+// maximum Q = 6 or 4) on n values v with random words w; out receives the
+// signed grid values.  All arrays are fp32 / uint32 on the device.
+NVFP4_API int nvfp4_test_sr_round(const float* v_dev, const uint32_t* w_dev, int64_t n, float Q, float* out_dev,
+                                  void* stream) {
+  if (!v_dev || !w_dev || !out_dev) return NVFP4_ERR_NULL;
+  if (n < 0 || (Q != 6.0f && Q != 4.0f)) return NVFP4_ERR_SHAPE;
+  if (!aligned(v_dev, 4) || !aligned(w_dev, 4) || !aligned(out_dev, 4)) return NVFP4_ERR_ALIGN;
+  if (n == 0) return NVFP4_OK;
+  const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  nvfp4::sr_round_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(v_dev, w_dev, n, Q,
+                                                                                          out_dev);
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -291,6 +291,61 @@ def test_device_philox_equals_curand():
     assert differ == 0 and differ_sign == 0
 
 
+def _sr_cases(Q, rng):
+    """Values and words for the stochastic rounding: random values on both
+    sides of the grid and beyond Q, zeros, subnormals and tiny normals, and
+    for values in every step region the words just below, at and above the
+    decision boundary k = p * 2^24 (k = w >> 8, p the fraction of the step)."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    v = [rng.uniform(-8.0, 8.0, 40000), np.exp2(rng.uniform(-30, 3, 40000)) * rng.choice([-1.0, 1.0], 40000),
+         np.array([0.0, -0.0, 2.0 ** -149, -(2.0 ** -149), 2.0 ** -126, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                   Q, -Q, Q + 0.25, 7.99, 100.0, -1e30]), grid, -grid, grid[1:] - 2.0 ** -20]
+    v = np.concatenate(v).astype(np.float32)
+    w = rng.integers(0, 2 ** 32, v.size, dtype=np.uint64).astype(np.uint32)
+    # boundary words: m from each region, k in {ceil(P) - 1, ceil(P), floor(P)} with P = p * 2^24
+    m = np.concatenate([rng.uniform(0.0, 0.5, 3000), rng.uniform(0.5, 1.0, 3000), rng.uniform(1.0, Q, 6000),
+                        np.exp2(rng.uniform(-40, -1, 3000))]).astype(np.float32)
+    bv, bw = [], []
+    for mm in m.astype(np.float64):
+        lo = grid[np.searchsorted(grid, mm, side="right") - 1]
+        hi = grid[min(np.searchsorted(grid, mm, side="right"), grid.size - 1)]
+        if hi == lo:
+            continue
+        P = (mm - lo) / (hi - lo) * 2.0 ** 24          # exact in double
+        for k in {int(np.ceil(P)) - 1, int(np.ceil(P)), int(np.floor(P))}:
+            if 0 <= k < 2 ** 24:
+                bv.append(mm)
+                bw.append((k << 8) | int(rng.integers(0, 256)))
+    v = np.concatenate([v, np.array(bv, np.float32)])
+    w = np.concatenate([w, np.array(bw, np.uint32)])
+    return v, w
+
+
+@pytest.mark.parametrize("Q", [6.0, 4.0])
+def test_device_stochastic_rounding_equals_the_oracle(Q):
+    """The kernels' stochastic rounding (run alone through the test-only
+    library, same device code) gives the oracle's grid value, with the sign
+    of the input, on random values, zeros, subnormals, values beyond Q, and
+    words on both sides of and exactly at every decision boundary."""
+    import ctypes
+    hook = selftest_lib().nvfp4_test_sr_round
+    hook.restype = ctypes.c_int
+    hook.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
+                     ctypes.c_void_p]
+    v, w = _sr_cases(Q, np.random.default_rng(20260 + int(Q)))
+    vd = torch.from_numpy(v).cuda()
+    wd = torch.from_numpy(w.view(np.int32)).cuda()
+    out = torch.empty_like(vd)
+    assert hook(vd.data_ptr(), wd.data_ptr(), v.size, Q, out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    m = np.minimum(np.abs(v), np.float32(Q))
+    ref = np.array([oracle.e2m1_value(oracle.round_sr(float(mm), int(ww))) for mm, ww in zip(m, w)], np.float32)
+    ref = np.copysign(ref, v)
+    bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+    assert bad.size == 0, [(float(v[i]), hex(int(w[i])), float(got[i]), float(ref[i])) for i in bad[:5]]
+
+
 def test_tile_copy_timeout_is_reported_and_the_context_stays_usable():
     """The 1D quantize kernel in a variant whose tile copies are never issued
     (test-only library: the barriers are armed, nothing arrives) stops after
