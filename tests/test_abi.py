@@ -210,6 +210,14 @@ def test_self_check_hooks_reject_bad_arguments():
     assert rh(ALIGNED, 16, 16, 16, 0, 0, ALIGNED2 + 2, None) == -3  # out not 4-byte aligned
     assert qc(ALIGNED + 4, None) == -3                              # 64-bit counters need 8 bytes
     assert ph(ALIGNED + 4, 16, None) == -3
+    sr = L.nvfp4_test_sr_round
+    sr.restype = ctypes.c_int
+    sr.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    assert sr(None, ALIGNED, 4, 6.0, ALIGNED2, None) == -1
+    assert sr(ALIGNED, ALIGNED, -1, 6.0, ALIGNED2, None) == -2      # negative count
+    assert sr(ALIGNED, ALIGNED, 4, 5.0, ALIGNED2, None) == -2       # Q other than 6 or 4
+    assert sr(ALIGNED + 2, ALIGNED, 4, 4.0, ALIGNED2, None) == -3   # values not 4-byte aligned
+    assert sr(ALIGNED, ALIGNED, 0, 6.0, ALIGNED2, None) == 0        # nothing to do, nothing launched
     nc = L.nvfp4_test_quantize_no_copy
     nc.restype = ctypes.c_int
     nc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 8
