@@ -61,12 +61,14 @@ WORKLOAD_CHOICES = list(COMPOSITES) + list(synthetic.WORKLOADS)
 
 # Integer-multiply roofline of the stochastic-rounding kernels: a Philox4x32-10
 # call takes ten rounds of two 32x32->64-bit products; with the counter's
-# upper words zero, the first round's second product is a product with zero
-# and the last round's first product feeds only the unused words 2 and 3, so
-# 18 products per call depend on the counter.  A 64-bit-result integer
-# multiply issues at a quarter of the 128 lanes per clock of an SM (measured:
-# 28.7-29.7 products per clock per SM for mul.wide.u32 and mul.hi.u32).
-PHILOX_PRODUCTS_PER_CALL = 18
+# upper words zero, the first round's second product is a product with zero,
+# the second round's first product depends only on the counter's high word
+# (shared by every element of a block) and the last round's first product
+# feeds only the unused words 2 and 3, so 17 products per call depend on the
+# element.  A 64-bit-result integer multiply issues at a quarter of the 128
+# lanes per clock of an SM (measured: 28.7-29.7 products per clock per SM for
+# mul.wide.u32 and mul.hi.u32).
+PHILOX_PRODUCTS_PER_CALL = 17
 WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 
 # DRAM bytes (read + written) of one launch of a kernel from an ncu capture,

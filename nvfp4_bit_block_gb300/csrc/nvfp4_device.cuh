@@ -181,6 +181,68 @@ __device__ __forceinline__ uint2 philox_w01(uint32_t c0, uint32_t c1, uint32_t k
   return make_uint2(c0, c1);
 }
 
+// The same words for a counter (lo, hi, 0, 0) whose second-round product of
+// word 0, M0 * (hi ^ k0), is given: in the first round word 2 is zero, so
+// word 0 leaves it as hi ^ k0 and word 1 as zero, and that product depends
+// on the high word and the key alone -- counters that share a high word
+// share it.
+__device__ __forceinline__ uint2 philox_w01_shared_hi(uint32_t lo, uint64_t p0_round1, uint32_t k0, uint32_t k1) {
+  const uint64_t q = (uint64_t)0xD2511F53u * lo;  // round 0
+  uint32_t c2 = (uint32_t)(q >> 32) ^ k1;
+  uint32_t c3 = (uint32_t)q;
+  k0 += 0x9E3779B9u;
+  k1 += 0xBB67AE85u;
+  const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;  // round 1
+  uint32_t c0 = (uint32_t)(p1 >> 32) ^ k0;
+  uint32_t c1 = (uint32_t)p1;
+  c2 = (uint32_t)(p0_round1 >> 32) ^ c3 ^ k1;
+  c3 = (uint32_t)p0_round1;
+  k0 += 0x9E3779B9u;
+  k1 += 0xBB67AE85u;
+#pragma unroll
+  for (int round = 2; round < 10; ++round) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1r = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1r >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1r;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint2(c0, c1);
+}
+
+// Words 0 and 1 of the NC counters base + j * stride, j = 0..NC-1
+// (stride < 2^32).  When all of them share their high word -- every group but
+// one that crosses a multiple of 2^32 -- the second-round product of word 0 is
+// formed once for the group.
+template <int NC, bool W1>
+__device__ __forceinline__ void philox_group_w01(uint64_t base, uint32_t stride, uint32_t k0, uint32_t k1,
+                                                 uint32_t* w0, uint32_t* w1) {
+  const uint64_t last = base + (uint64_t)(NC - 1) * stride;
+  if ((uint32_t)(base >> 32) == (uint32_t)(last >> 32)) {
+    const uint64_t p0r1 = (uint64_t)0xD2511F53u * ((uint32_t)(base >> 32) ^ k0);
+    const uint32_t lo = (uint32_t)base;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const uint2 r = philox_w01_shared_hi(lo + (uint32_t)j * stride, p0r1, k0, k1);
+      w0[j] = r.x;
+      if (W1) w1[j] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const uint64_t i = base + (uint64_t)j * stride;
+      const uint2 r = philox_w01((uint32_t)i, (uint32_t)(i >> 32), k0, k1);
+      w0[j] = r.x;
+      if (W1) w1[j] = r.y;
+    }
+  }
+}
+
 // RHT sign bits: word 0 of Philox(key = seed, counter = (0,0,0,1)).
 __device__ __forceinline__ uint32_t rht_sign_bits(uint32_t k0, uint32_t k1) {
   uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 1u;

@@ -52,8 +52,6 @@ __device__ __forceinline__ uint32_t stash_off(int r, int c) {
   return (uint32_t)r * 1024u + (uint32_t)((q ^ ((q >> 3) & 7) ^ ((r & 1) << 1)) << 4) + (uint32_t)(c & 3) * 4u;
 }
 
-__device__ __forceinline__ uint2 ctr_of(uint64_t i) { return make_uint2((uint32_t)i, (uint32_t)(i >> 32)); }
-
 // Per-copy scale constants: den = Q*alpha and its correctly rounded
 // reciprocal for Q = 6 and Q = 4, and the shared (d, 1/d) table of alpha.
 struct CopyScales {
@@ -332,15 +330,8 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
         block_bytes<Q46>(bmax, scR, e6, e4);
         uint32_t w[16];
         if (SR) {
-          const uint64_t base = ct + (uint64_t)(64 * k);
           uint32_t w1[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint2 c = ctr_of(base + j);
-            const uint2 pw = philox_w01(c.x, c.y, a.sr_k0, a.sr_k1);
-            w[j] = pw.x;
-            w1[j] = pw.y;
-          }
+          philox_group_w01<16, kStash>(ct + (uint64_t)(64 * k), 1u, a.sr_k0, a.sr_k1, w, w1);
           if (kStash) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -420,12 +411,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
               for (int i = 0; i < 16; ++i)
                 w[i] = *reinterpret_cast<const uint32_t*>(stash + stash_off(16 * rb + i, cc));
             } else {
-              const uint64_t base = a.ctr_off + (uint64_t)((R0 + 16 * rb) * N + C0 + cc);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const uint2 ct = ctr_of(base + (uint64_t)i * (uint64_t)N);
-                w[i] = philox_w01(ct.x, ct.y, a.sr_k0, a.sr_k1).y;
-              }
+              uint32_t w0[16];
+              philox_group_w01<16, true>(a.ctr_off + (uint64_t)((R0 + 16 * rb) * N + C0 + cc), (uint32_t)N, a.sr_k0,
+                                 a.sr_k1, w0, w);
             }
           }
           quant_block16<Q46, SR, SEL>(zz[h], scC, w, e6[h], e4[h], codes[h], es[h]);

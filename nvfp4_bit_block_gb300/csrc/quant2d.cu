@@ -30,9 +30,10 @@ using tile::kTM;
 using tile::kTN;
 constexpr int kBlockThreads = 256;
 
-__device__ __forceinline__ uint32_t word0_of(const QuantArgs& a, int64_t r, int64_t c) {
-  const uint64_t i = a.ctr_off + (uint64_t)r * (uint64_t)a.N + (uint64_t)c;
-  return philox_w01((uint32_t)i, (uint32_t)(i >> 32), a.sr_k0, a.sr_k1).x;
+// Philox word 0 of the eight elements (r, c .. c+7) (counter = element index).
+__device__ __forceinline__ void words0_of8(const QuantArgs& a, int64_t r, int64_t c, uint32_t* w) {
+  philox_group_w01<8, false>(a.ctr_off + (uint64_t)r * (uint64_t)a.N + (uint64_t)c, 1u, a.sr_k0, a.sr_k1, w,
+                             nullptr);
 }
 
 // Scaled (and, for SR, rounded) value of one element at block scale s.
@@ -219,10 +220,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : 3)
         float z[8];
         patch_row(pbase, pc, i, z);
         uint32_t w[8];
-        if (SR) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[j] = word0_of(a, grow0 + i, gcol0 + j);
-        }
+        if (SR) words0_of8(a, grow0 + i, gcol0, w);
         const float p6 = cand8<SR, SEL>(z, s, 6.0f, w, code6[i]);
         const float p4 = cand8<SR, SEL>(z, s4, 4.0f, w, code4[i]);
         r6[i] = err_combine(p6, __shfl_xor_sync(0xFFFFFFFFu, p6, 1), SEL);
@@ -254,8 +252,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : 3)
           float z[8], v[8];
           patch_row(pbase, pc, i, z);
           if (SR) {
+            uint32_t w[8];
+            words0_of8(a, grow0 + i, gcol0, w);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = scaled<true>(z[j], s, 6.0f, word0_of(a, grow0 + i, gcol0 + j));
+            for (int j = 0; j < 8; ++j) v[j] = scaled<true>(z[j], s, 6.0f, w[j]);
           } else {
             const float2 inv2 = make_float2(s.inv, s.inv);
 #pragma unroll

@@ -193,7 +193,10 @@ namespace nvfp4 {
 namespace {
 
 // out[0] = counters whose words 0/1 differ from cuRAND's, out[1] = keys whose
-// 16 RHT sign bits (low half of word 0) differ, out[2] = cases checked.  Thread t of the grid takes
+// 16 RHT sign bits (low half of word 0) differ, out[2] = cases checked,
+// out[3] = counters where the form with the second-round product given
+// differs, out[4] = words of 16-counter blocks that differ, out[5] = blocks
+// checked that cross a multiple of 2^32.  Thread t of the grid takes
 // counter (c0, c1) and key (k0, k1) from a hash of t; the first 4096 threads
 // take counter and key words from {0, 1, 2^31, 2^32 - 1} instead, so that
 // carries and all-ones words are covered.
@@ -221,6 +224,24 @@ __global__ void philox_check_kernel(unsigned long long* out) {
   const uint2 ours = philox_w01(c0, c1, k0, k1);
   const uint4 ref = curand_Philox4x32_10(make_uint4(c0, c1, 0u, 0u), make_uint2(k0, k1));
   if (ours.x != ref.x || ours.y != ref.y) atomicAdd(out + 0, 1ull);
+  // the form with the second-round product given, and the 16-counter form
+  // (stride 1 or a hashed stride; the extreme words make blocks that cross a
+  // multiple of 2^32)
+  const uint2 sh = philox_w01_shared_hi(c0, (uint64_t)0xD2511F53u * (c1 ^ k0), k0, k1);
+  if (sh.x != ref.x || sh.y != ref.y) atomicAdd(out + 3, 1ull);
+  const uint32_t stride = (t & 1u) ? 1u : (mix32(t * 0x165667B1u) >> 12);
+  const uint64_t base = (((uint64_t)c1 << 32) | c0) - ((t & 2u) ? 7ull * stride : 0ull);
+  uint32_t w0[16], w1[16];
+  philox_group_w01<16, true>(base, stride, k0, k1, w0, w1);
+  unsigned long long bad16 = 0;
+#pragma unroll 1
+  for (int j = 0; j < 16; ++j) {
+    const uint64_t i = base + (uint64_t)j * stride;
+    const uint4 r = curand_Philox4x32_10(make_uint4((uint32_t)i, (uint32_t)(i >> 32), 0u, 0u), make_uint2(k0, k1));
+    if (w0[j] != r.x || w1[j] != r.y) ++bad16;
+  }
+  if (bad16) atomicAdd(out + 4, bad16);
+  if ((base >> 32) != ((base + 15ull * stride) >> 32)) atomicAdd(out + 5, 1ull);
   const uint4 ref_sign = curand_Philox4x32_10(make_uint4(0u, 0u, 0u, 1u), make_uint2(k0, k1));
   if (rht_sign_bits(k0, k1) != (ref_sign.x & 0xFFFFu)) atomicAdd(out + 1, 1ull);  // 16 signs: low half of word 0
   atomicAdd(out + 2, 1ull);
@@ -233,7 +254,7 @@ extern "C" {
 
 // Test hook (not declared in nvfp4.h): compare the kernels' Philox4x32-10 with
 // cuRAND's over `blocks` x 256 counter/key cases (blocks >= 16 covers the
-// extreme words).  out_dev: three zeroed unsigned 64-bit counters (see above).
+// extreme words).  out_dev: six zeroed unsigned 64-bit counters (see above).
 NVFP4_API int nvfp4_test_philox_check(unsigned long long* out_dev, int blocks, void* stream) {
   if (!out_dev) return NVFP4_ERR_NULL;
   if (!aligned(out_dev, 8)) return NVFP4_ERR_ALIGN;

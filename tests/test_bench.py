@@ -40,8 +40,8 @@ def test_default_workload_is_the_full_linear_layer():
 
 
 def test_philox_roofline_peak_from_unit_counts():
-    """152 SMs x 32 wide products per clock / 18 products per call x 2070 MHz."""
-    assert abs(bench.philox_peak_gcalls(152, 2070.0) - 152 * 32 / 18 * 2.07) < 1e-9
+    """152 SMs x 32 wide products per clock / 17 products per call x 2070 MHz."""
+    assert abs(bench.philox_peak_gcalls(152, 2070.0) - 152 * 32 / 17 * 2.07) < 1e-9
 
 
 def test_traffic_is_null_for_a_stale_capture(monkeypatch):

@@ -278,17 +278,22 @@ def test_scale_quotient_equals_ieee_division_exhaustively():
 def test_device_philox_equals_curand():
     """The kernels' Philox4x32-10 (stochastic-rounding words 0 and 1, RHT sign
     word) equals cuRAND's device implementation of the generator on 2^20
-    counter/key cases, including every combination of extreme words."""
+    counter/key cases, including every combination of extreme words; so do
+    the form that takes the second-round product shared by one high word,
+    and the 16-counter blocks the kernels draw (stride 1 and larger strides,
+    some blocks crossing a multiple of 2^32)."""
     import ctypes
     hook = selftest_lib().nvfp4_test_philox_check
     hook.restype = ctypes.c_int
     hook.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
-    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    out = torch.zeros(6, dtype=torch.int64, device="cuda")
     assert hook(out.data_ptr(), 4096, None) == 0
     torch.cuda.synchronize()
-    differ, differ_sign, checked = out.cpu().tolist()
+    differ, differ_sign, checked, differ_shared, differ16, crossing = out.cpu().tolist()
     assert checked == 4096 * 256
     assert differ == 0 and differ_sign == 0
+    assert differ_shared == 0 and differ16 == 0
+    assert crossing > 100  # blocks of 16 counters across a multiple of 2^32 were among them
 
 
 def _sr_cases(Q, rng):
