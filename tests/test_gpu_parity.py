@@ -200,6 +200,29 @@ def test_swizzled_scales_are_the_plain_scales_relaid(flags):
             assert np.array_equal(gs[f"s_{which}"], relayout_tiled(g[f"s_{which}"]))
 
 
+@pytest.mark.parametrize("flags,sel", [(ROW | COL, 0), (ROW | COL | F46, 1), (ROW | COL | RHT_COL | SR, 0),
+                                       (ROW | F46 | SR, 2), (COL, 0)])
+def test_more_tiles_than_one_round(flags, sel):
+    """A 1984 x 4096 tensor has 496 tiles of 64 x 256: more than one round of
+    the persistent grid on 152 SMs at three or two CTAs per SM, and not a
+    multiple of either, so CTAs walk different numbers of tiles.  Every code
+    and scale byte equals the oracle's, and the tiled scale layout is the
+    plain one relaid."""
+    M, N = 1984, 4096
+    assert torch.cuda.get_device_properties(0).multi_processor_count * 3 < (M // 64) * (N // 256)
+    bits = small_input(M, N, kind="grad" if flags & SR else "act")
+    x = to_device(bits)
+    g = gpu_quantize(x, flags, sel, sr_seed=21, rht_seed=22, counter_offset=5)
+    r = ref_quantize(bits, flags, sel, sr_seed=21, rht_seed=22, counter_offset=5)
+    assert_parity(g, r, flags)
+    gs = gpu_quantize(x, flags | nv.SF_SWIZZLED, sel, sr_seed=21, rht_seed=22, counter_offset=5)
+    for which in ("row", "col"):
+        if g[f"q_{which}"] is None:
+            continue
+        assert np.array_equal(gs[f"q_{which}"], g[f"q_{which}"])
+        assert np.array_equal(gs[f"s_{which}"], relayout_tiled(g[f"s_{which}"]))
+
+
 @pytest.mark.parametrize("scale", [1.75, 0.4])
 def test_caller_supplied_amax_single_pass(scale):
     """Delayed scaling: nvfp4_quantize with an amax the caller supplies (here a
