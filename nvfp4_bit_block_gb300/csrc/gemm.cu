@@ -38,19 +38,38 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBM = 128, kBN = 128;
+constexpr int kBM = 128;
 constexpr int kBK = 256;                         // FP4 values per K step (128 bytes of codes per row)
-constexpr int kStages = 6;
 constexpr int kTileA = kBM * kBK / 2;            // 16 KB
-constexpr int kTileB = kBN * kBK / 2;            // 16 KB
 constexpr int kSfBlock = 512;                    // scales of 128 rows x 64 values
-constexpr int kSfBytes = (kBK / 64) * kSfBlock;  // 2 KB per operand and stage
-constexpr int kStageBytes = kTileA + kTileB + 2 * kSfBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers, TMEM address */ + 1024 /* alignment */;
-constexpr uint32_t kTmemCols = 512;              // accumulators 0-255, scale factors 256-447
-constexpr uint32_t kSfCol0 = 256;
+constexpr int kSfBytes = (kBK / 64) * kSfBlock;  // 2 KB per 128 rows and stage
+constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 320;
 constexpr int kSfWarp0 = 6;  // warps 6-9 move the scale blocks to TMEM
+
+// Tile shapes: 128 x 128 output tiles with two accumulators (the epilogue of
+// one tile overlaps the next tile's MMAs) and six stages, or 128 x 256 tiles
+// with one accumulator and four stages -- a quarter fewer operand bytes per
+// FLOP through shared memory, for an epilogue that the next tile's MMAs wait
+// for until it has read the accumulator out (its stores overlap them only
+// after the last chunk).  TMEM: accumulators in columns 0-255,
+// per-stage scale factors from column 256 (A: 4 columns per MMA; B: 4 per
+// 128 rows per MMA).
+template <int BN>
+struct Cfg {
+  static constexpr int kBN = BN;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kAcc = BN == 256 ? 1 : 2;
+  static constexpr int kTileB = BN * kBK / 2;              // 16 / 32 KB
+  static constexpr int kSfbBytes = (BN / 128) * kSfBytes;  // 2 / 4 KB
+  static constexpr int kStageBytes = kTileA + kTileB + kSfBytes + kSfbBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers, TMEM address */ + 1024 /* alignment */;
+  static constexpr uint32_t kSfCol0 = kAcc * BN;           // 256
+  static constexpr uint32_t kSfbCols = 4 * (BN / 128);     // per MMA
+  static constexpr uint32_t kSfStageCols = 16 + 4 * kSfbCols;
+  static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "TMEM columns");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,8 +98,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages, kStageBytes = C::kStageBytes, kTileB = C::kTileB, kAcc = C::kAcc;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nk = (int)(a.K / kBK);
-  const int64_t tiles_n = a.N / kBN, tiles_m = a.M / kBM, tiles = tiles_m * tiles_n;
+  const int64_t tiles_n = a.N / BN, tiles_m = a.M / kBM, tiles = tiles_m * tiles_n;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -129,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t tm, tn;
         tile_coords(t, tiles_m, tiles_n, tm, tn);
         const uint8_t* sfa = a.sfa + tm * sf_tiles_k * kSfBlock;
-        const uint8_t* sfb = a.sfb + tn * sf_tiles_k * kSfBlock;
+        const uint8_t* sfb = a.sfb + tn * (BN / 128) * sf_tiles_k * kSfBlock;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = (int)(g % kStages);
           const uint32_t ph = (uint32_t)(g / kStages) & 1u;
@@ -141,22 +163,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = full0 + 8 * s;
           tma::arrive_expect_tx(full, kStageBytes);
           tma::load_2d(smem_u32(st), &amap, kb * (kBK / 2), (int)(tm * kBM), full);
-          tma::load_2d(smem_u32(st + kTileA), &bmap, kb * (kBK / 2), (int)(tn * kBN), full);
+          tma::load_2d(smem_u32(st + kTileA), &bmap, kb * (kBK / 2), (int)(tn * BN), full);
           tc5::bulk_g2s(smem_u32(st + kTileA + kTileB), sfa + (int64_t)kb * kSfBytes, kSfBytes, full);
-          tc5::bulk_g2s(smem_u32(st + kTileA + kTileB + kSfBytes), sfb + (int64_t)kb * kSfBytes, kSfBytes, full);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)  // B's 128-row bands: their scale blocks one after the other
+            tc5::bulk_g2s(smem_u32(st + kTileA + kTileB + kSfBytes + h * kSfBytes),
+                          sfb + h * sf_tiles_k * kSfBlock + (int64_t)kb * kSfBytes, kSfBytes, full);
         }
       }
+      // No copy may still be landing in shared memory when the CTA exits: the
+      // last fill of every stage has completed (the MMA thread waited for it)
+      // unless the pipeline stopped early, so wait for those fills (bounded).
+      for (int64_t j = (g > kStages ? g - kStages : 0); j < g; ++j)
+        tma::wait(full0 + 8 * (int)(j % kStages), (uint32_t)(j / kStages) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer
-      constexpr uint32_t idesc = tc5::idesc_e2m1_e4m3(kBM, kBN);
+      constexpr uint32_t idesc = tc5::idesc_e2m1_e4m3(kBM, BN);
       int64_t g = 0;
       int li = 0;  // tiles of this CTA
       for (int64_t t = blockIdx.x; t < tiles && !*abort_v; t += gridDim.x, ++li) {
-        const int ab = li & 1;
-        const uint32_t acc = tmem + (uint32_t)(ab * kBN);
-        if (li >= 2 && !tma::wait(acce0 + 8 * ab, (uint32_t)((li >> 1) & 1) ^ 1u)) {
+        const int ab = li % kAcc, use = li / kAcc;
+        const uint32_t acc = tmem + (uint32_t)(ab * BN);
+        // the epilogue has read this accumulator's previous tile out
+        if (use >= 1 && !tma::wait(acce0 + 8 * ab, (uint32_t)((use - 1) & 1))) {
           *abort_v = 1;
           break;
         }
@@ -172,10 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc5::fence_after_thread_sync();
           const uint8_t* st = smem + s * kStageBytes;
           const uint32_t a_base = smem_u32(st), b_base = smem_u32(st + kTileA);
+          const uint32_t sf_base = tmem + C::kSfCol0 + (uint32_t)(s * C::kSfStageCols);
 #pragma unroll
           for (int j = 0; j < kBK / 64; ++j) {
-            const uint32_t sfa_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 4 * j);
-            const uint32_t sfb_t = tmem + kSfCol0 + (uint32_t)(s * 32 + 16 + 4 * j);
+            const uint32_t sfa_t = sf_base + (uint32_t)(4 * j);
+            const uint32_t sfb_t = sf_base + 16u + C::kSfbCols * (uint32_t)j;
             // K step j: 64 values = 32 bytes into each 128-byte swizzled row
             const uint64_t adesc = tc5::smem_desc(a_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
             const uint64_t bdesc = tc5::smem_desc(b_base + 32 * j, 16, 1024, tc5::kLayoutSwizzle128B);
@@ -190,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSfWarp0) {
     // scale warps: warp w writes TMEM lane quarter w % 4; every quarter gets the
-    // same 16 bytes per lane (the four row groups of the 128 x 4 scale tile)
+    // same 16 bytes per lane (the four row groups of a 128 x 4 scale tile)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     int64_t g = 0;
     bool stop = false;  // warp-uniform: every lane takes the same path to the .sync.aligned stores
@@ -206,12 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* sf = smem + s * kStageBytes + kTileA + kTileB;
+        const uint32_t sf_base = tmem + lane_base + C::kSfCol0 + (uint32_t)(s * C::kSfStageCols);
 #pragma unroll
         for (int j = 0; j < kBK / 64; ++j) {
           const uint4 va = *reinterpret_cast<const uint4*>(sf + j * kSfBlock + 16 * lane);
-          const uint4 vb = *reinterpret_cast<const uint4*>(sf + kSfBytes + j * kSfBlock + 16 * lane);
-          tc5::st_32x32b_x4(tmem + lane_base + kSfCol0 + (uint32_t)(s * 32 + 4 * j), va);
-          tc5::st_32x32b_x4(tmem + lane_base + kSfCol0 + (uint32_t)(s * 32 + 16 + 4 * j), vb);
+          tc5::st_32x32b_x4(sf_base + (uint32_t)(4 * j), va);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const uint4 vb = *reinterpret_cast<const uint4*>(sf + kSfBytes + h * kSfBytes + j * kSfBlock + 16 * lane);
+            tc5::st_32x32b_x4(sf_base + 16u + C::kSfbCols * (uint32_t)j + 4u * h, vb);
+          }
         }
         tc5::wait_st();
         tc5::fence_before_thread_sync();
@@ -225,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = __fmul_rn(a.alpha_a[0], a.alpha_b[0]);
     int li = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++li) {
-      const int ab = li & 1;
-      const bool ready = tma::wait(accf0 + 8 * ab, (uint32_t)((li >> 1) & 1));
+      const int ab = li % kAcc, use = li / kAcc;
+      const bool ready = tma::wait(accf0 + 8 * ab, (uint32_t)(use & 1));
       // warp-uniform decision before the .sync.aligned TMEM loads
       if (!__all_sync(0xFFFFFFFFu, ready) || __any_sync(0xFFFFFFFFu, *abort_v != 0)) {
         if (lane == 0) *abort_v = 1;
@@ -236,18 +272,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t tm, tn;
       tile_coords(t, tiles_m, tiles_n, tm, tn);
       const int64_t row = tm * kBM + 32 * q + lane;
-      const uint32_t acc = tmem + (uint32_t)(ab * kBN) + ((uint32_t)(32 * q) << 16);
+      const uint32_t acc = tmem + (uint32_t)(ab * BN) + ((uint32_t)(32 * q) << 16);
+      auto release = [&]() {  // the accumulator is in registers: hand it back to the MMA warp
+        tc5::fence_before_thread_sync();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8 * ab) : "memory");
+      };
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tc5::ld_32x32b_x32(acc + (uint32_t)(32 * c), r);
         tc5::wait_ld();
-        if (c == kBN / 32 - 1) {  // the accumulator is in registers: hand it back
-          tc5::fence_before_thread_sync();
-          __syncwarp();
-          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8 * ab) : "memory");
-        }
-        const int64_t col = tn * kBN + 32 * c;
+        if (c == BN / 32 - 1) release();
+        const int64_t col = tn * BN + 32 * c;
         if (a.out_bf16) {
           uint16_t* dst = reinterpret_cast<uint16_t*>(a.d) + row * a.ldd + col;
 #pragma unroll
@@ -284,22 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tc5::dealloc(tmem, kTmemCols);
 }
 
-}  // namespace
-
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+template <int BN>
+cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
+  using C = Cfg<BN>;
   static std::atomic<int> grid_cap[64] = {};
   int cap = 0;
-  const cudaError_t ge = resident_grid(gemm_nvf4_kernel, kThreads, kSmemBytes, grid_cap, cap);
+  const cudaError_t ge = resident_grid(gemm_nvf4_kernel<BN>, kThreads, C::kSmemBytes, grid_cap, cap);
   if (ge != cudaSuccess) return ge;
   CUtensorMap amap, bmap;
   cudaError_t e = make_codes_map(&amap, a.qa, a.M, a.K / 2, kBK / 2, kBM);
   if (e != cudaSuccess) return e;
-  e = make_codes_map(&bmap, a.qb, a.N, a.K / 2, kBK / 2, kBN);
+  e = make_codes_map(&bmap, a.qb, a.N, a.K / 2, kBK / 2, BN);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = (a.M / kBM) * (a.N / kBN);
+  const int64_t tiles = (a.M / kBM) * (a.N / BN);
   const int64_t grid = tiles < cap ? tiles : cap;
-  gemm_nvf4_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, amap, bmap);
+  gemm_nvf4_kernel<BN><<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(a, amap, bmap);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// 128 x 256 tiles when N allows them, else 128 x 128.
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+  return (a.N % 256 == 0) ? launch_gemm_bn<256>(a, s) : launch_gemm_bn<128>(a, s);
 }
 
 }  // namespace nvfp4

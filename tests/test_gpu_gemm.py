@@ -74,11 +74,14 @@ def test_gemm_single_tile_one_k_step():
     check(128, 128, 256)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (128, 256, 2048), (384, 128, 4096), (2048, 3072, 512)])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (128, 256, 2048), (384, 128, 4096), (2048, 3072, 512),
+                                   (2048, 2560, 768)])
 def test_gemm_tiles_and_pipeline_stages(M, N, K):
-    """Several output tiles per CTA (the last shape has more tiles than SMs,
-    so both TMEM accumulators take turns), and K spanning more K steps than
-    pipeline stages."""
+    """Both tile widths (128 x 256 where N is a multiple of 256, else
+    128 x 128), several output tiles per CTA (the last two shapes have more
+    tiles than SMs: the accumulators are reused, and with three K steps per
+    tile the four-stage ring wraps within a CTA's second tile), and K
+    spanning more K steps than pipeline stages."""
     check(M, N, K, seed=M + N + K)
 
 
