@@ -839,7 +839,7 @@ def main():
                                    "flags": workload_config(args, p)[0], "selection": workload_config(args, p)[1]}
                                   for p in parts]}
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "config": config,
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cb["sample"]},
