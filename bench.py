@@ -73,8 +73,15 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 
 # DRAM bytes (read + written) of one launch of a kernel from an ncu capture,
 # keyed by (tensor, kernel) with the hash of the kernel sources the capture was
-# taken on; a stale hash reports null.
-TRAFFIC = {}
+# taken on; a stale hash reports null.  Captured with
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
+#       -k regex:quant1d -c 1 python bench.py --once --workload <tensor>
+# (one pass; a cold single launch, so outputs still in L2 at its end are not
+# counted as written).
+TRAFFIC = {
+    ("linear_dy_16384x20480", "quantize"): (694_680_000 + 366_300_000, "7464e5e8437a44d7"),
+    ("grad_rht_sr_16384x5120", "quantize"): (168_110_000 + 61_130_000, "7464e5e8437a44d7"),
+}
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
 
