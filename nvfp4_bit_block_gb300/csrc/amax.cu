@@ -40,7 +40,13 @@ __device__ __forceinline__ uint32_t packed_to_bits(uint32_t m) {
   return max(m << 16, m & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+// NaN-propagating maximum of m and |v| (for non-negative m, the same order as
+// the bit patterns of the magnitudes: NaN above Inf above every finite value)
+__device__ __forceinline__ float max_abs_nan(float m, float v) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
+  return r;
+}
 
 // CTA-wide max of two values, then one atomicMax each.
 __device__ __forceinline__ void cta_reduce_and_publish(uint32_t vr, uint32_t vc, float* amax) {
@@ -93,7 +99,8 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
   const uint32_t signs = (RHT_ROW || RHT_COL) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
   const int rb_b = tid & 15, rb_r0 = tid >> 4;    // rowwise tasks
   const int cp_p = tid & 127, cp_rb0 = tid >> 7;  // columnwise tasks
-  uint32_t m_plain = 0u, m_row = 0u, m_col = 0u;
+  uint32_t m_plain = 0u;
+  float m_row = 0.0f, m_col = 0.0f;
 
   tile::Walker w;
   w.init(M, N);
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
           for (int i = 0; i < 16; ++i) zp[i] = bf16x2_to_f32x2(wd[i] ^ rht_mask_col(signs, i));
           wht16_x2(zp);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m_col = max(m_col, max(abs_bits(zp[i].x), abs_bits(zp[i].y)));
+          for (int i = 0; i < 16; ++i) m_col = max_abs_nan(max_abs_nan(m_col, zp[i].x), zp[i].y);
         }
       }
     }
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
         }
         wht16(z);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) m_row = max(m_row, abs_bits(z[j]));
+        for (int j = 0; j < 16; ++j) m_row = max_abs_nan(m_row, z[j]);
       }
     }
     __syncthreads();  // the buffer is refilled by the next iteration's prefetch
@@ -160,8 +167,8 @@ __global__ void __launch_bounds__(kBlockThreads) amax_tile_kernel(const AmaxArgs
   const uint32_t plain = packed_to_bits(m_plain);
   // max |y| = max |t| / 4 for the unnormalised butterfly output t: the scaling
   // is exact and rounding is monotonic, so it commutes with the maximum
-  const uint32_t quarter_row = __float_as_uint(__fmul_rn(__uint_as_float(m_row), 0.25f));
-  const uint32_t quarter_col = __float_as_uint(__fmul_rn(__uint_as_float(m_col), 0.25f));
+  const uint32_t quarter_row = __float_as_uint(__fmul_rn(m_row, 0.25f));
+  const uint32_t quarter_col = __float_as_uint(__fmul_rn(m_col, 0.25f));
   cta_reduce_and_publish(RHT_ROW ? quarter_row : plain, RHT_COL ? quarter_col : plain, a.amax);
 }
 

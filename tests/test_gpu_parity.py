@@ -119,21 +119,27 @@ def test_zero_and_empty_tensors():
 
 
 def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
-    for pattern, want in ((0x7F80, -6), (0xFFC0, -6)):
-        bits = synthetic.weight(32, 32, 1)
-        bits[5, 7] = pattern
-        x = to_device(bits)
-        amax = nv.nvfp4_amax(x, ROW | COL)
-        out = nv.Quantized(*(torch.full(s, 0xAB, dtype=torch.uint8, device="cuda")
-                             for s in nv.output_shapes(32, 32, ROW | COL)),
-                           alpha=torch.zeros(2, device="cuda"), status=torch.zeros(1, dtype=torch.int32,
-                                                                                   device="cuda"))
-        nv.nvfp4_quantize(x, amax, ROW | COL, out=out)
-        torch.cuda.synchronize()
-        assert out.status.item() == want
-        assert bool((out.q_row == 0xAB).all()) and bool((out.s_col == 0xAB).all())
-        st, am = oracle.amax(bits, ROW | COL)
-        assert oracle.quantize(bits, 32, am, ROW | COL)["status"] == want
+    """An Inf or NaN anywhere makes the amax (plain, or of the Hadamard-
+    transformed copy) non-finite; the quantize then reports NONFINITE and
+    writes nothing."""
+    for flags in (ROW | COL, ROW | COL | RHT_COL, ROW | COL | RHT_ROW | RHT_COL):
+        for pattern, want in ((0x7F80, -6), (0xFFC0, -6)):
+            bits = synthetic.weight(32, 32, 1)
+            bits[5, 7] = pattern
+            x = to_device(bits)
+            amax = nv.nvfp4_amax(x, flags)
+            out = nv.Quantized(*(torch.full(s, 0xAB, dtype=torch.uint8, device="cuda")
+                                 for s in nv.output_shapes(32, 32, flags)),
+                               alpha=torch.zeros(2, device="cuda"), status=torch.zeros(1, dtype=torch.int32,
+                                                                                       device="cuda"))
+            nv.nvfp4_quantize(x, amax, flags, out=out)
+            torch.cuda.synchronize()
+            assert out.status.item() == want
+            assert not np.isfinite(amax.cpu().numpy()).any()
+            assert bool((out.q_row == 0xAB).all()) and bool((out.s_col == 0xAB).all())
+            st, am = oracle.amax(bits, flags)
+            assert not np.isfinite(am).any()
+            assert oracle.quantize(bits, 32, am, flags)["status"] == want
     tiny = np.full((32, 32), 0x0001, np.uint16)
     g = gpu_quantize(to_device(tiny), ROW)
     assert g["status"] == -7
