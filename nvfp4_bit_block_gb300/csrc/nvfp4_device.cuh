@@ -310,8 +310,9 @@ __device__ __forceinline__ BlockScale block_scale(float b, float alpha, float Q)
 // fl(b / den).  That is not always fl(b / den) itself, but its E4M3 byte is
 // the byte of fl(b / den) for every pair of a finite bf16 block maximum and an
 // accepted bf16 amax, for fp32 amax values between them and for random fp32
-// maxima -- checked exhaustively on the device (selftest.cu); the bare product
-// gets tens of thousands of those bytes wrong.
+// maxima -- checked exhaustively on the device by the test-only self-check
+// library (tests/selftest); the bare product gets tens of thousands of those
+// bytes wrong.
 // b >= 0 finite, den > 0 normal, or den == rden == 0 with b == 0.
 __device__ __forceinline__ float quotient_rn(float b, float den, float rden) {
   const float q = __fmul_rn(b, rden);

@@ -1,7 +1,7 @@
 // tcgen05.cuh -- fifth-generation tensor core (tcgen05) instructions of
 // sm_100a / sm_103a used by the NVFP4 GEMM, as inline PTX: tensor memory
 // (TMEM) allocation, block-scaled MMA with E2M1 operands and E4M3 scale
-// factors, shared-memory -> TMEM copies of the scale factors, completion
+// factors, register -> TMEM stores of the scale factors, completion
 // tracking on an mbarrier, and TMEM -> register loads for the epilogue.
 //
 // Shared-memory matrix descriptor (64 bits): start address >> 4 in bits 0-13,
@@ -21,7 +21,6 @@
 namespace nvfp4 {
 namespace tc5 {
 
-constexpr uint32_t kLayoutNone = 0;
 constexpr uint32_t kLayoutSwizzle128B = 2;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
@@ -63,12 +62,6 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint6
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1u : 0u)
       : "memory");
-}
-
-// 32 rows x 16 bytes of shared memory (described by `src`) into 4 TMEM
-// columns of lanes 0-31, replicated to the four 32-lane quarters.
-__device__ __forceinline__ void cp_32x128b_warpx4(uint32_t taddr, uint64_t src) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
 }
 
 // The mbarrier at `bar` receives one arrival when every tcgen05 operation

@@ -252,7 +252,7 @@ def test_caller_supplied_amax_single_pass(scale):
 @pytest.mark.parametrize("along_cols", [0, 1])
 def test_transformed_values_agree_with_the_oracle(along_cols):
     """The tolerance on transformed values: the kernels' fp32 Hadamard
-    transform (run alone through a test hook, same device code) agrees with
+    transform (run alone through the test-only library, same device code) agrees with
     the oracle's (double precision, rounded once) within 1e-6 of each
     16-vector's 2-norm, for vectors along rows and along columns."""
     import ctypes
