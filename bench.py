@@ -79,8 +79,8 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize"): (694_680_000 + 366_300_000, "7464e5e8437a44d7"),
-    ("grad_rht_sr_16384x5120", "quantize"): (168_110_000 + 61_130_000, "7464e5e8437a44d7"),
+    ("linear_dy_16384x20480", "quantize"): (694_030_000 + 365_300_000, "7bd70281787646b6"),
+    ("grad_rht_sr_16384x5120", "quantize"): (168_080_000 + 61_340_000, "7bd70281787646b6"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
