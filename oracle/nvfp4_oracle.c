@@ -308,7 +308,8 @@ int nvfp4ref_amax(const uint16_t* x, int64_t M, int64_t N, int64_t ld, uint32_t 
 }
 
 /* Philox words for element (r, c) of the source tensor: counter = element
- * index (north-star reading of "counter = element index"), key = seed. */
+ * index (the counter_offset plus the element's row-major index in the
+ * source tensor), key = seed. */
 static void element_words(uint64_t sr_seed, uint64_t counter_offset, int64_t N, int64_t r, int64_t c,
                           uint32_t out[4]) {
   uint64_t i = counter_offset + (uint64_t)r * (uint64_t)N + (uint64_t)c;

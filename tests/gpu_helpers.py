@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
 binding, run the oracle on the same seeded input, and compare.
 
-Bar (from the benchmark spec's tolerances):
+Bar (the method's stated tolerances):
 * no Hadamard transform on a copy: amax, alpha, every code byte and every scale
   byte bit-exact;
 * Hadamard-transformed copy: amax and alpha within 1e-6 relative; at most
