@@ -450,7 +450,7 @@ def run_ours(args, rank: int, world: int):
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->nvfp4 (fp32 arithmetic)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, the recipe's shapes and value distributions)",
         "config": config,
         "kernels_ms": {f"{r['tensor']}:{r['kernel']}": r["ms"] for r in kernels},
