@@ -82,3 +82,28 @@ def test_all_cores_oracle_run_covers_the_tensor():
     assert r["kind"] == "oracle" and r["value"] > 0
     assert 1 <= r["cores"] <= min(len(os.sched_getaffinity(0)), 256 // 16)
     assert "256x1024" in r["sample"]
+
+
+@pytest.mark.gpu
+def test_benchmark_line_on_the_gpu():
+    """The benchmark's own arm on a GPU (the small rowwise workload, two
+    steps): one JSON line with the contract's keys, a roofline for the
+    dominant kernel, the end-to-end figure with the bytes it moved, the
+    single-pass figure, the clocks and the launch count."""
+    lines = run_bench("--workload", "rowwise_rn_256x1024", "--steps", "3", "--warmup", "3",
+                      "--no-cpu-baseline", env={"CUDA_VISIBLE_DEVICES": os.environ.get("CUDA_VISIBLE_DEVICES", "0")})
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks",
+                "single_pass", "kernels"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["dtype"] == "f32"
+    assert d["config"]["workload"] == "rowwise_rn_256x1024"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    r = d["roofline"]
+    assert r["bound"] in ("hbm", "alu") and 0 < r["frac"] and r["achieved"] > 0 and r["peak"] > 0
+    assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 2 * 256 * 1024
+    assert d["e2e"]["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 2 * 3  # amax and quantize per step
+    assert d["clocks"]["sm_mhz"] is None or d["clocks"]["sm_mhz"] > 0
