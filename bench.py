@@ -72,32 +72,41 @@ PHILOX_PRODUCTS_PER_CALL = 17
 WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 
 # DRAM bytes (read + written) of one launch of a kernel from an ncu capture,
-# keyed by (tensor, kernel) with the hash of the kernel sources the capture was
-# taken on; a stale hash reports null.  Captured with
+# keyed by (tensor, kernel) with the hash of that kernel's sources
+# (KERNEL_SOURCES) when the capture was taken; a stale hash reports null.  Captured with
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
 #       -k regex:quant1d -c 1 python bench.py --once --workload <tensor>
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize"): (694_030_000 + 365_300_000, "7bd70281787646b6"),
-    ("grad_rht_sr_16384x5120", "quantize"): (168_080_000 + 61_340_000, "7bd70281787646b6"),
+    ("linear_dy_16384x20480", "quantize"): (694_030_000 + 365_300_000, "bfdf313a0c1d0f9d"),
+    ("grad_rht_sr_16384x5120", "quantize"): (168_080_000 + 61_340_000, "bfdf313a0c1d0f9d"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
 
-def source_hash() -> str:
-    """Hash of the CUDA sources of the product library (16 hex digits)."""
+# The CUDA sources each kernel of the step is built from (a traffic capture
+# stays valid while these are unchanged).
+KERNEL_SOURCES = {
+    "quantize": ["api.cu", "tmap.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
+                 "quant1d_kernel.cuh", "quant2d.cu", "tile_pipeline.cuh", "tma.cuh", "nvfp4_device.cuh",
+                 "nvfp4_internal.h"],
+    "amax": ["api.cu", "amax.cu", "tile_pipeline.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
+}
+
+
+def source_hash(kernel: str = "quantize") -> str:
+    """Hash of the CUDA sources `kernel` is built from (16 hex digits)."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_of(part: str, kernel: str):
     entry = TRAFFIC.get((part, kernel))
-    if entry is None or entry[1] != source_hash():
+    if entry is None or entry[1] != source_hash(kernel):
         return None
     return entry[0]
 

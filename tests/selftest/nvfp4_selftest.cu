@@ -25,13 +25,15 @@
 // an independent one, over pseudo-random and extreme counters and keys.  A
 // fourth launches the 1D quantize kernel in a variant that arms its tile
 // barriers but issues no copy, so that the bounded wait runs out.  A fifth
-// runs the kernels' stochastic rounding alone on given values and words.
+// runs the kernels' stochastic rounding alone on given values and words, and
+// a sixth launches the GEMM in a variant whose copies are never issued.
 #include <cstdint>
 
 #include <curand_philox4x32_x.h>
 
 #include "nvfp4.h"
 #include "nvfp4_device.cuh"
+#include "gemm_kernel.cuh"
 #include "quant1d_kernel.cuh"
 
 namespace {
@@ -327,6 +329,43 @@ NVFP4_API int nvfp4_test_sr_round(const float* v_dev, const uint32_t* w_dev, int
   nvfp4::sr_round_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(v_dev, w_dev, n, Q,
                                                                                           out_dev);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+// Test hook: the NVFP4 GEMM in a variant whose producer arms the stage
+// barriers but issues no copy, so every wait runs out: the kernel writes
+// NVFP4_ERR_PIPELINE to status_dev after about a second, drains and frees its
+// tensor memory, and returns.  Arguments as nvfp4_gemm; all pointers are
+// required.
+NVFP4_API int nvfp4_test_gemm_no_copy(const uint8_t* qa, const uint8_t* sfa, const float* alpha_a, const uint8_t* qb,
+                                      const uint8_t* sfb, const float* alpha_b, void* d, int64_t M, int64_t N,
+                                      int64_t K, int64_t ldd, int out_bf16, int* status_dev, void* stream) {
+  if (!qa || !sfa || !alpha_a || !qb || !sfb || !alpha_b || !d || !status_dev) return NVFP4_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256 || ldd < N) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(d, 16) ||
+      !aligned(alpha_a, 4) || !aligned(alpha_b, 4) || !aligned(status_dev, 4) || ldd % (out_bf16 ? 8 : 4))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::GemmArgs a{};
+  a.qa = qa;
+  a.sfa = sfa;
+  a.alpha_a = alpha_a;
+  a.qb = qb;
+  a.sfb = sfb;
+  a.alpha_b = alpha_b;
+  a.d = d;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldd = ldd;
+  a.out_bf16 = out_bf16;
+  a.status = status_dev;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (N % 256 == 0) ? nvfp4::gemmk::launch<256, true>(a, s) : nvfp4::gemmk::launch<128, true>(a, s);
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // extern "C"

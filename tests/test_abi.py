@@ -218,6 +218,15 @@ def test_self_check_hooks_reject_bad_arguments():
     assert sr(ALIGNED, ALIGNED, 4, 5.0, ALIGNED2, None) == -2       # Q other than 6 or 4
     assert sr(ALIGNED + 2, ALIGNED, 4, 4.0, ALIGNED2, None) == -3   # values not 4-byte aligned
     assert sr(ALIGNED, ALIGNED, 0, 6.0, ALIGNED2, None) == 0        # nothing to do, nothing launched
+    gn = L.nvfp4_test_gemm_no_copy
+    gn.restype = ctypes.c_int
+    gn.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    gok = [ALIGNED, ALIGNED2, ALIGNED3, ALIGNED, ALIGNED2, ALIGNED3, ALIGNED, 128, 256, 256, 256, 1, ALIGNED3, None]
+    gcall = lambda changes: gn(*[changes.get(i, v) for i, v in enumerate(gok)])
+    assert gcall({0: None}) == -1 and gcall({12: None}) == -1        # operands, status required
+    assert gcall({7: 100}) == -2 and gcall({9: 128}) == -2           # M % 128, K % 256
+    assert gcall({10: 128}) == -2                                    # ldd < N
+    assert gcall({0: ALIGNED + 8}) == -3 and gcall({10: 260}) == -3  # qa alignment, ldd % 8 with bf16
     nc = L.nvfp4_test_quantize_no_copy
     nc.restype = ctypes.c_int
     nc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 8

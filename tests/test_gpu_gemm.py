@@ -98,3 +98,27 @@ def test_gemm_rejects_bad_shapes_and_alignment():
         nv.nvfp4_gemm(q[:100], s, al, q, s, al)                    # M % 128
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemm(q[:, :64], s, al, q[:, :64], s, al)          # K = 128 < 256
+
+
+@pytest.mark.parametrize("N", [256, 384])
+def test_gemm_wait_timeout_is_reported_and_the_context_stays_usable(N):
+    """The GEMM in a variant whose operand copies are never issued (test-only
+    library; both tile widths): every bounded wait runs out, the kernel
+    reports NVFP4_ERR_PIPELINE, drains and frees its tensor memory, and the
+    next GEMM on the same context is correct."""
+    import ctypes
+    from gpu_helpers import selftest_lib
+    hook = selftest_lib().nvfp4_test_gemm_no_copy
+    hook.restype = ctypes.c_int
+    hook.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    M, K = 256, 512
+    A, _ = operand(M, K, 31)
+    B, _ = operand(N, K, 32)
+    d = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hook(A.q_row.data_ptr(), A.s_row.data_ptr(), A.alpha[0:1].data_ptr(), B.q_row.data_ptr(),
+                B.s_row.data_ptr(), B.alpha[0:1].data_ptr(), d.data_ptr(), M, N, K, N, 0, status.data_ptr(),
+                None) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == -8
+    check(M, N, K, seed=33)  # the context is usable and the product kernel correct
