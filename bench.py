@@ -79,8 +79,8 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize"): (694_030_000 + 365_300_000, "bfdf313a0c1d0f9d"),
-    ("grad_rht_sr_16384x5120", "quantize"): (168_080_000 + 61_340_000, "bfdf313a0c1d0f9d"),
+    ("linear_dy_16384x20480", "quantize"): (689_100_000 + 362_220_000, "7a75695b8271c2ac"),
+    ("grad_rht_sr_16384x5120", "quantize"): (167_875_328 + 56_585_216, "7a75695b8271c2ac"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
@@ -89,8 +89,8 @@ CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 # stays valid while these are unchanged).
 KERNEL_SOURCES = {
     "quantize": ["api.cu", "tmap.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
-                 "quant1d_kernel.cuh", "quant2d.cu", "tile_pipeline.cuh", "tma.cuh", "nvfp4_device.cuh",
-                 "nvfp4_internal.h"],
+                 "quant1d_kernel.cuh", "quant1d_sr.cu", "quant1d_sr_kernel.cuh", "quant2d.cu", "tile_pipeline.cuh",
+                 "tma.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
     "amax": ["api.cu", "amax.cu", "tile_pipeline.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
 }
 

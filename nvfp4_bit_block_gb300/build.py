@@ -23,7 +23,7 @@ SELFTEST_DIR = os.path.join(ROOT, "tests", "selftest")
 SELFTEST_BUILD = os.path.join(SELFTEST_DIR, "_build")
 SELFTEST_LIB = os.path.join(SELFTEST_BUILD, "libnvfp4_selftest.so")
 
-SOURCES = ["api.cu", "tmap.cu", "amax.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
+SOURCES = ["api.cu", "tmap.cu", "amax.cu", "quant1d.cu", "quant1d_sr.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
            "quant2d.cu", "dequant.cu", "analysis.cu", "gemm.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -102,6 +102,8 @@ cudaError_t resident_grid(Kernel kern, int threads, int smem, std::atomic<int>* 
 
 cudaError_t launch_amax(const AmaxArgs& a, bool rht_row, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d(const QuantArgs& a, bool row, bool col, bool q46, bool sr, cudaStream_t s);
+// rowwise + columnwise, stochastic rounding, no 4/6, Hadamard on the columnwise copy or none
+cudaError_t launch_quant1d_sr_rc(const QuantArgs& a, bool rht_col, cudaStream_t s);
 cudaError_t launch_quant1d_46_mae(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
 cudaError_t launch_quant1d_46_mse(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);
 cudaError_t launch_quant1d_46_max(const QuantArgs& a, bool row, bool col, bool sr, cudaStream_t s);

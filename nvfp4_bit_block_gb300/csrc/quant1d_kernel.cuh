@@ -17,10 +17,12 @@
 // quotient_rn), the RHT flags and the 4/6 rule are template parameters.
 //
 // With stochastic rounding on both copies, one Philox4x32-10 call per element
-// serves both: the rowwise pass uses word 0 and parks word 1 in shared memory
-// for the columnwise pass (that 64 KB stash leaves room for one tile buffer,
-// so those kernels load each tile after the previous one is done and rely on
-// their second CTA per SM for overlap).
+// serves both.  Without 4/6 and without a rowwise Hadamard transform that
+// case runs in quant1d_sr_kernel.cuh (both roundings in the columnwise pass);
+// here, for 4/6 or a rowwise transform, the rowwise pass uses word 0 and
+// parks word 1 in shared memory for the columnwise pass (that 64 KB stash
+// leaves room for one tile buffer, so those kernels load each tile after the
+// previous one is done and rely on their second CTA per SM for overlap).
 //
 // Sources: "Four Over Six (4/6)" technical summary (Problem statement,
 // Methodology, Implementation details) and "Pretraining Large Language Models
@@ -169,6 +171,27 @@ __device__ __forceinline__ void quant_block16(const float* z, const CopyScales& 
   e = four ? e4 : e6;
 }
 
+// a2 and the checks every 1D kernel makes first: alpha of each copy (block 0
+// writes both), the status of each produced copy's amax, and the 1 KB
+// alignment of the dynamic shared memory that the 128-byte swizzle needs.
+// False when the kernel must stop; block 0 has recorded why.
+__device__ __forceinline__ bool begin_tensor(const QuantArgs& a, bool row, bool col, float den, const uint8_t* smem,
+                                             float& alpha_r, float& alpha_c) {
+  const float A_r = a.amax[0], A_c = a.amax[1];
+  alpha_r = __fdiv_rn(A_r, den);
+  alpha_c = __fdiv_rn(A_c, den);
+  const int st_r = row ? amax_status(A_r) : 0;
+  const int st_c = col ? amax_status(A_c) : 0;
+  const bool misaligned = (tile::smem_u32(smem) & 1023u) != 0u;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    a.alpha[0] = alpha_r;
+    a.alpha[1] = alpha_c;
+    if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
+    if (misaligned && !(st_r || st_c) && a.status) *a.status = kStatusPipeline;
+  }
+  return !(st_r || st_c || misaligned);
+}
+
 // Scale bytes of a block with maximum b (e4 only with 4/6).
 template <bool Q46>
 __device__ __forceinline__ void block_bytes(float b, const CopyScales& sc, uint32_t& e6, uint32_t& e4) {
@@ -198,20 +221,8 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
   const uint32_t bar0 = tile::smem_u32(tbl + 127), bar1 = tile::smem_u32(tbl + 255);
 
   // a2: alpha = amax / (6*448), or amax / (6*256) with 4/6
-  const float den = Q46 ? kAlphaDen46 : kAlphaDen;
-  const float A_r = a.amax[0], A_c = a.amax[1];
-  const float alpha_r = __fdiv_rn(A_r, den);
-  const float alpha_c = __fdiv_rn(A_c, den);
-  const int st_r = ROW ? amax_status(A_r) : 0;
-  const int st_c = COL ? amax_status(A_c) : 0;
-  const bool misaligned = (tile::smem_u32(smem) & 1023u) != 0u;  // the 128-byte swizzle needs 1 KB alignment
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    a.alpha[0] = alpha_r;
-    a.alpha[1] = alpha_c;
-    if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
-    if (misaligned && !(st_r || st_c) && a.status) *a.status = kStatusPipeline;
-  }
-  if (st_r || st_c || misaligned) return;
+  float alpha_r, alpha_c;
+  if (!begin_tensor(a, ROW, COL, Q46 ? kAlphaDen46 : kAlphaDen, smem, alpha_r, alpha_c)) return;
 
   const int64_t M = a.M, N = a.N;
   const int tid = threadIdx.x;
@@ -450,9 +461,15 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Stochastic rounding on both copies without 4/6 and without a rowwise
+// Hadamard transform runs in quant1d_sr_kernel (launch_quant1d_sr_rc).
 template <bool ROW, bool COL, bool Q46, int SEL, int RHT>
 cudaError_t launch_sr(const QuantArgs& a, bool sr, cudaStream_t s) {
-  return sr ? launch<ROW, COL, Q46, true, SEL, RHT>(a, s) : launch<ROW, COL, Q46, false, SEL, RHT>(a, s);
+  if constexpr (ROW && COL && !Q46 && (RHT & 1) == 0) {
+    return sr ? launch_quant1d_sr_rc(a, RHT == 2, s) : launch<ROW, COL, Q46, false, SEL, RHT>(a, s);
+  } else {
+    return sr ? launch<ROW, COL, Q46, true, SEL, RHT>(a, s) : launch<ROW, COL, Q46, false, SEL, RHT>(a, s);
+  }
 }
 
 // All row/column/SR/RHT combinations of one (4/6, selection rule) pair.

@@ -23,8 +23,9 @@
 // compares the kernels' Philox4x32-10 (the stochastic-rounding words and the
 // RHT sign word) with cuRAND's device implementation of the same generator,
 // an independent one, over pseudo-random and extreme counters and keys.  A
-// fourth launches the 1D quantize kernel in a variant that arms its tile
-// barriers but issues no copy, so that the bounded wait runs out.  A fifth
+// fourth launches a 1D quantize kernel (round-to-nearest, or stochastic
+// rounding on both copies) in a variant that arms its tile barriers but
+// issues no copy, so that the bounded wait runs out.  A fifth
 // runs the kernels' stochastic rounding alone on given values and words, and
 // a sixth launches the GEMM in a variant whose copies are never issued.
 #include <cstdint>
@@ -35,6 +36,7 @@
 #include "nvfp4_device.cuh"
 #include "gemm_kernel.cuh"
 #include "quant1d_kernel.cuh"
+#include "quant1d_sr_kernel.cuh"
 
 namespace {
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -269,14 +271,15 @@ NVFP4_API int nvfp4_test_philox_check(unsigned long long* out_dev, int blocks, v
 
 extern "C" {
 
-// Test hook: the rowwise + columnwise round-to-nearest 1D quantize kernel in
-// a variant whose tile barriers are armed but whose copies are never issued,
-// so every wait runs out: the kernel writes NVFP4_ERR_PIPELINE to status_dev
-// after about a second and returns.  Arguments as nvfp4_quantize with flags
-// ROWWISE | COLWISE; all pointers are required.
+// Test hook: a rowwise + columnwise 1D quantize kernel in a variant whose
+// tile barriers are armed but whose copies are never issued, so every wait
+// runs out: the kernel writes NVFP4_ERR_PIPELINE to status_dev after about a
+// second and returns.  sr = 0: the round-to-nearest kernel (flags ROWWISE |
+// COLWISE); sr = 1: the stochastic-rounding kernel (ROWWISE | COLWISE | SR).
+// Other arguments as nvfp4_quantize; all pointers are required.
 NVFP4_API int nvfp4_test_quantize_no_copy(const void* x_dev, int64_t M, int64_t N, int64_t ld, const float* amax_dev,
                                           uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                                          float* alpha_dev, int* status_dev, void* stream) {
+                                          float* alpha_dev, int* status_dev, int sr, void* stream) {
   if (!x_dev || !amax_dev || !q_row || !s_row || !q_col || !s_col || !alpha_dev || !status_dev) return NVFP4_ERR_NULL;
   if (M <= 0 || N <= 0 || M % 16 || N % 16 || ld < N || M > INT32_MAX || N > INT32_MAX) return NVFP4_ERR_SHAPE;
   if (ld % 8 || !aligned(x_dev, 16) || !aligned(q_row, 16) || !aligned(q_col, 16) || !aligned(s_row, 4) ||
@@ -295,8 +298,10 @@ NVFP4_API int nvfp4_test_quantize_no_copy(const void* x_dev, int64_t M, int64_t 
   a.q_col = q_col;
   a.s_col = s_col;
   a.sel = nvfp4::kSelMAE;
-  const cudaError_t e =
-      nvfp4::q1d::launch<true, true, false, false, nvfp4::kSelMAE, 0, true>(a, static_cast<cudaStream_t>(stream));
+  if (sr != 0 && sr != 1) return NVFP4_ERR_FLAGS;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = sr ? nvfp4::q1d::launch_sr_rc<false, true>(a, s)
+                           : nvfp4::q1d::launch<true, true, false, false, nvfp4::kSelMAE, 0, true>(a, s);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

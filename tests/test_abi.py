@@ -229,10 +229,12 @@ def test_self_check_hooks_reject_bad_arguments():
     assert gcall({0: ALIGNED + 8}) == -3 and gcall({10: 260}) == -3  # qa alignment, ldd % 8 with bf16
     nc = L.nvfp4_test_quantize_no_copy
     nc.restype = ctypes.c_int
-    nc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 8
-    ok = [ALIGNED, 64, 256, 256, ALIGNED2, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED3, ALIGNED3, None]
+    nc.argtypes = ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 7 +
+                   [ctypes.c_int, ctypes.c_void_p])
+    ok = [ALIGNED, 64, 256, 256, ALIGNED2, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED3, ALIGNED3, 0, None]
     call = lambda changes: nc(*[changes.get(i, v) for i, v in enumerate(ok)])
     assert call({0: None}) == -1 and call({10: None}) == -1         # x, status required
     assert call({1: 24}) == -2 and call({2: 24, 3: 24}) == -2       # M % 16, N % 16
     assert call({3: 128}) == -2                                     # ld < N
     assert call({0: ALIGNED + 8}) == -3 and call({5: ALIGNED + 4}) == -3
+    assert call({11: 2}) == -4                                      # sr other than 0 or 1

@@ -380,28 +380,33 @@ def test_device_stochastic_rounding_equals_the_oracle(Q):
     assert bad.size == 0, [(float(v[i]), hex(int(w[i])), float(got[i]), float(ref[i])) for i in bad[:5]]
 
 
-def test_tile_copy_timeout_is_reported_and_the_context_stays_usable():
-    """The 1D quantize kernel in a variant whose tile copies are never issued
-    (test-only library: the barriers are armed, nothing arrives) stops after
-    its bounded wait and reports NVFP4_ERR_PIPELINE in the status word; the
-    next call on the same context is correct."""
+@pytest.mark.parametrize("sr", [0, 1], ids=["rn", "sr"])
+def test_tile_copy_timeout_is_reported_and_the_context_stays_usable(sr):
+    """A 1D quantize kernel (round-to-nearest, or stochastic rounding on both
+    copies) in a variant whose tile copies are never issued (test-only
+    library: the barriers are armed, nothing arrives) stops after its bounded
+    wait and reports NVFP4_ERR_PIPELINE in the status word; the next call on
+    the same context is correct."""
     import ctypes
     hook = selftest_lib().nvfp4_test_quantize_no_copy
     hook.restype = ctypes.c_int
-    hook.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 8
-    bits = synthetic.weight(64, 256, 3)  # a single tile
+    hook.argtypes = ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 7 +
+                     [ctypes.c_int, ctypes.c_void_p])
+    flags = ROW | COL | (SR if sr else 0)
+    M = 64
+    bits = synthetic.weight(M, 256, 3)  # a single tile
     x = to_device(bits)
-    amax = nv.nvfp4_amax(x, ROW | COL)
-    out = nv.nvfp4_quantize(x, amax, ROW | COL)  # allocates the outputs
+    amax = nv.nvfp4_amax(x, flags)
+    out = nv.nvfp4_quantize(x, amax, flags)  # allocates the outputs
     out.status.zero_()
     torch.cuda.synchronize()
     p = lambda t: t.data_ptr()
-    assert hook(p(x), 64, 256, 256, p(amax), p(out.q_row), p(out.s_row), p(out.q_col), p(out.s_col), p(out.alpha),
-                p(out.status), torch.cuda.current_stream().cuda_stream) == 0
+    assert hook(p(x), M, 256, 256, p(amax), p(out.q_row), p(out.s_row), p(out.q_col), p(out.s_col), p(out.alpha),
+                p(out.status), sr, torch.cuda.current_stream().cuda_stream) == 0
     torch.cuda.synchronize()
     assert out.status.item() == -8
     assert nv.nvfp4_strerror(-8).startswith("a tile copy")
-    assert_parity(gpu_quantize(x, ROW | COL), ref_quantize(bits, ROW | COL), ROW | COL)
+    assert_parity(gpu_quantize(x, flags, sr_seed=5), ref_quantize(bits, flags, sr_seed=5), flags)
 
 
 def test_two_d_copies_are_transposes_and_dequantize_identically():
