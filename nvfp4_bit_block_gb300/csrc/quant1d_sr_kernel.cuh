@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       for (int i = 0; i < 16; ++i)
         wd[i] = *reinterpret_cast<const uint32_t*>(cb + i * 128 + (c_chunk ^ ((uint32_t)(i & 7) << 4)));
       // columnwise values and maxima (low half = column 2p, high half = 2p+1)
-      float2 y[RHT_COL ? 16 : 1];
+      float2 y[16];  // with RHT_COL: the transformed columnwise values
       float bm0, bm1;
       if (RHT_COL) {
 #pragma unroll
@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
         for (int j = 0; j < kChunkRows; ++j) {
           const int i = I0 + j;
           const float2 x = bf16x2_to_f32x2(wd[i]);
-          const float2 yc = RHT_COL ? y[RHT_COL ? i : 0] : x;
+          float2 yc = x;
+          if constexpr (RHT_COL) yc = y[i];
           const float ir = ri[i];
           const float2 vr = mul2(x, make_float2(ir, ir));
           const float2 vc = mul2(yc, invc);
