@@ -79,8 +79,8 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize"): (689_100_000 + 362_220_000, "7a75695b8271c2ac"),
-    ("grad_rht_sr_16384x5120", "quantize"): (167_875_328 + 56_585_216, "7a75695b8271c2ac"),
+    ("linear_dy_16384x20480", "quantize"): (689_300_000 + 362_100_000, "c92d1c10c07e76f1"),
+    ("grad_rht_sr_16384x5120", "quantize"): (167_860_000 + 56_300_000, "c92d1c10c07e76f1"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
