@@ -43,6 +43,14 @@ using tile::kTM;
 using tile::kTN;
 constexpr int kStashBytes = kTM * kTN * 4;  // Philox word 1 per element, 64 KB
 constexpr int kBlockThreads = 256;
+// Tile width (columns) of the 1D kernel: 64 x 128 tiles for plain
+// round-to-nearest, whose CTAs are bound by the latency of a tile's work (a
+// narrower tile halves it, and with it the cost of the launch's first and
+// last rounds of tiles: RN R+C 32.6 -> 30.7 us on 8192 x 5120); 64 x 256
+// with 4/6, RHT or SR (the narrow tile measured 1-9 % slower there, and the
+// SR stash is laid out for 256 columns).
+template <bool Q46, bool SR, int RHT>
+constexpr int tile_width() { return (Q46 || SR || RHT != 0) ? kTN : kTN / 2; }
 
 // Byte offset of the stash word of tile row r, tile column c.  A row is
 // 1 KB (256 words); its 16-byte chunk q = c / 4 sits at
@@ -211,8 +219,9 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
   // per SM; a single buffer fits two, whose loads overlap each other's math.
   constexpr bool kDB = !kStash;
   constexpr int kBufs = kDB ? 2 : 1;
-  uint8_t* bufs = smem;                                      // 1 or 2 x 32 KB tiles (1024-aligned)
-  uint8_t* cstage = smem + kBufs * tile::kTileBytes;         // 8 KB
+  constexpr int kTW = tile_width<Q46, SR, RHT>(), kTileBytes = kTM * kTW * 2, kBoxes = kTW / 64;
+  uint8_t* bufs = smem;                                      // 1 or 2 tiles (1024-aligned)
+  uint8_t* cstage = smem + kBufs * kTileBytes;               // 8 KB
   uint8_t* sstage = cstage + tile::kCStageBytes;             // 1 KB
   float2* tbl = reinterpret_cast<float2*>(sstage + tile::kSStageBytes);  // 2 x 128 (d, 1/d)
   uint8_t* stash = reinterpret_cast<uint8_t*>(tbl + 256);    // 64 KB with kStash
@@ -228,13 +237,13 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
   const int tid = threadIdx.x;
   auto issue = [&](int b, const tile::Coord& c) {
     const uint32_t bar = b ? bar1 : bar0;
-    tma::arrive_expect_tx(bar, tile::kTileBytes);
+    tma::arrive_expect_tx(bar, kTileBytes);
     if (NOCOPY) return;
-    const uint32_t dst = tile::smem_u32(bufs + b * tile::kTileBytes);
+    const uint32_t dst = tile::smem_u32(bufs + b * kTileBytes);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
+    for (int j = 0; j < kBoxes; ++j) tma::load_2d(dst + j * 8192, &xmap, (int)c.C0 + 64 * j, (int)c.R0, bar);
   };
-  tile::Walker w;
+  tile::WalkerT<kTW> w;
   w.init(M, N);
   if (tid == 0) {
     tma::mbar_init(bar0, 1);
@@ -248,29 +257,32 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
   const CopyScales scC = make_scales(alpha_c, tbl + 128);
   const uint32_t signs = (kRhtRow || kRhtCol) ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
 
-  // Shared tile = four 64-column boxes as the TMA writes them: box j at
-  // 8 KB * j, row r at 128 * r, 16-byte chunk c at (c ^ (r & 7)) * 16.
+  // Shared tile = kTW / 64 boxes of 64 columns as the TMA writes them: box j
+  // at 8 KB * j, row r at 128 * r, 16-byte chunk c at (c ^ (r & 7)) * 16.
   // Fixed per-thread roles (relative to a tile's origin):
-  //  rowwise    tile row rr = 8*warp + lane/4, blocks rq + 4k (k = 0..3):
+  //  rowwise    tile row rr = 8*warp + lane/4, blocks rq + 4k (k < kTW/64):
   //             block rq + 4k is chunks 2rq, 2rq+1 of box k, so a quarter
   //             warp (rows rr, rr+1; four blocks each) hits eight distinct
   //             bank groups, and each row's four code words are 32 bytes
-  //  columnwise column pair cp_p, row blocks cp_rb0 + 2k (k = 0..1): a warp
+  //  columnwise column pair cp_p, row blocks cp_rb0 + kRbStep * k: a warp
   //             reads one 128-byte box row per load
   const int lane = tid & 31;
   const int rr = 8 * (tid >> 5) + (lane >> 2), rq = lane & 3;
   const uint32_t r_chunk0 = rr * 128 + ((uint32_t)((2 * rq) ^ (lane >> 2)) << 4);  // second chunk: ^ 16
   const int64_t hN = N / 2, sN = N / 16;
-  const int cp_p = tid & 127, cp_rb0 = tid >> 7;
+  constexpr int kPairs = kTW / 2;                    // column pairs of a tile
+  constexpr int kRbStep = kBlockThreads / kPairs;    // threads per column pair (row blocks apart)
+  constexpr int kColTasks = 4 / kRbStep;             // row blocks per thread
+  const int cp_p = tid % kPairs, cp_rb0 = tid / kPairs;
   const uint32_t c_base = (cp_p >> 5) * 8192 + (cp_p & 3) * 4;
   const uint32_t c_chunk = (uint32_t)((cp_p & 31) >> 2) << 4;
 
   for (int it = 0; w.valid(); w = w.next(), ++it) {
     const int b = kDB ? (it & 1) : 0;
-    uint8_t* buf = bufs + b * tile::kTileBytes;
+    uint8_t* buf = bufs + b * kTileBytes;
     if (tid == 0) {
       if (kDB) {
-        const tile::Walker wn = w.next();
+        const tile::WalkerT<kTW> wn = w.next();
         if (wn.valid()) issue(b ^ 1, wn.coord());  // that buffer was released by the last barrier
       } else if (it > 0) {
         issue(0, w.coord());
@@ -291,10 +303,10 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     const tile::Coord tc = w.coord();
     const int64_t R0 = tc.R0, C0 = tc.C0;
     const int rows = (int)((M - R0) < kTM ? (M - R0) : kTM);
-    const int cols = (int)((N - C0) < kTN ? (N - C0) : kTN);
+    const int cols = (int)((N - C0) < kTW ? (N - C0) : kTW);
     const bool cp_ok = 2 * cp_p < cols;
 
-    // ---- rowwise copy: one 16-column block per task, 4 tasks per thread
+    // ---- rowwise copy: one 16-column block per task, kBoxes tasks per thread
     if (ROW && rr < rows) {
       uint8_t* qt = a.q_row + (R0 + rr) * hN + C0 / 2 + 8 * rq;
       // scale of block rq + 4k: plain layout st + 4k; tiled layout st + 512k
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
       const int st_step = a.sf_swz ? 512 : 4;
       const uint64_t ct = a.ctr_off + (uint64_t)((R0 + rr) * N + C0 + 16 * rq);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // block rq + 4k of row rr
+      for (int k = 0; k < kBoxes; ++k) {  // block rq + 4k of row rr
         if (16 * (rq + 4 * k) >= cols) break;
         uint32_t wd[8];
         {
@@ -359,14 +371,14 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
     }
     if (kStash) __syncthreads();
 
-    // ---- columnwise copy: one column pair x 16 rows per task, 2 tasks per thread
+    // ---- columnwise copy: one column pair x 16 rows per task, kColTasks tasks per thread
     if (COL && cp_ok) {
       const int p = cp_p;
       // both tasks in flight at once, except with SR (its register budget is spent on Philox)
       constexpr int kColUnroll = SR ? 1 : 2;
 #pragma unroll kColUnroll
-      for (int k = 0; k < 2; ++k) {  // row block rb of column pair p (both columns)
-        const int rb = cp_rb0 + 2 * k;
+      for (int k = 0; k < kColTasks; ++k) {  // row block rb of column pair p (both columns)
+        const int rb = cp_rb0 + kRbStep * k;
         if (16 * rb >= rows) break;
         uint32_t wd[16];
         const uint8_t* cb = buf + c_base + rb * 2048;
@@ -433,14 +445,15 @@ __global__ void __launch_bounds__(kBlockThreads, SR ? 2 : NVFP4_Q1D_MIN_CTAS)
       }
     }
     __syncthreads();  // tile buffer free for the next copy; staging complete
-    if (COL) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid, a.sf_swz != 0);
+    if (COL && tid < kTW) tile::write_col_outputs(cstage, sstage, a.q_col, a.s_col, M, N, tc, tid, a.sf_swz != 0);
   }
 }
 
 template <bool ROW, bool COL, bool Q46, bool SR, int SEL, int RHT, bool NOCOPY = false>
 cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   constexpr bool kStash = SR && ROW && COL;
-  constexpr int kSmem = (kStash ? 1 : 2) * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
+  constexpr int kTW = tile_width<Q46, SR, RHT>();
+  constexpr int kSmem = (kStash ? 1 : 2) * (kTM * kTW * 2) + tile::kCStageBytes + tile::kSStageBytes + 256 * 8 +
                         (kStash ? kStashBytes : 0);
   auto kern = quant1d_kernel<ROW, COL, Q46, SR, SEL, RHT, NOCOPY>;
   // once per device: opt in to the dynamic shared memory and size the
@@ -450,7 +463,7 @@ cudaError_t launch(const QuantArgs& a, cudaStream_t s) {
   const cudaError_t ge = resident_grid(kern, kBlockThreads, kSmem, grid_cap, cap);
   if (ge != cudaSuccess) return ge;
   // persistent grid: every resident CTA slot, or one CTA per tile if fewer
-  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTN - 1) / kTN);
+  const int64_t ntiles = ((a.M + kTM - 1) / kTM) * ((a.N + kTW - 1) / kTW);
   int64_t g = ntiles < cap ? ntiles : cap;
   if (g < 1) g = 1;
   CUtensorMap xmap;

@@ -45,12 +45,15 @@ struct Coord {
 // Tile walk of a persistent CTA: tiles t = blockIdx.x + k*gridDim.x in
 // row-major tile order (ntx tiles per row of tiles), with the (row, column)
 // tile coordinates advanced incrementally instead of divided per tile.
-struct Walker {
+// TN: tile width in columns (the 1D kernels without stochastic rounding walk
+// 64 x 128 tiles).
+template <int TN = kTN>
+struct WalkerT {
   int64_t ty, tx;        // current tile
   int64_t step_y, step_x; // gridDim.x = step_y * ntx + step_x
   int64_t ntx, nty;
   __device__ __forceinline__ void init(int64_t M, int64_t N) {
-    ntx = (N + kTN - 1) / kTN;
+    ntx = (N + TN - 1) / TN;
     nty = (M + kTM - 1) / kTM;
     if (ntx < 1) ntx = 1;
     ty = blockIdx.x / ntx;
@@ -59,9 +62,9 @@ struct Walker {
     step_x = gridDim.x - step_y * ntx;
   }
   __device__ __forceinline__ bool valid() const { return ty < nty; }
-  __device__ __forceinline__ Coord coord() const { return {ty * kTM, tx * kTN}; }
-  __device__ __forceinline__ Walker next() const {
-    Walker w = *this;
+  __device__ __forceinline__ Coord coord() const { return {ty * kTM, tx * TN}; }
+  __device__ __forceinline__ WalkerT next() const {
+    WalkerT w = *this;
     w.tx += step_x;
     w.ty += step_y;
     if (w.tx >= ntx) {
@@ -71,6 +74,7 @@ struct Walker {
     return w;
   }
 };
+using Walker = WalkerT<>;
 
 // Issue the async copies of one tile (NT threads, thread `tid`).
 template <int NT>
