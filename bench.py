@@ -75,12 +75,12 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 # keyed by (tensor, kernel) with the hash of that kernel's sources
 # (KERNEL_SOURCES) when the capture was taken; a stale hash reports null.  Captured with
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
-#       -k regex:quant1d -c 1 python bench.py --once --workload <tensor>
+#       -k regex:quant1d_sr -c 1 python bench.py --once --workload <tensor>
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize"): (689_300_000 + 362_100_000, "c92d1c10c07e76f1"),
-    ("grad_rht_sr_16384x5120", "quantize"): (167_860_000 + 56_300_000, "c92d1c10c07e76f1"),
+    ("linear_dy_16384x20480", "quantize_sr"): (689_220_000 + 362_040_000, "6960f11f7896163a"),
+    ("grad_rht_sr_16384x5120", "quantize_sr"): (167_860_000 + 56_610_000, "6960f11f7896163a"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
@@ -89,8 +89,12 @@ CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 # stays valid while these are unchanged).
 KERNEL_SOURCES = {
     "quantize": ["api.cu", "tmap.cu", "quant1d.cu", "quant1d_46mae.cu", "quant1d_46mse.cu", "quant1d_46max.cu",
-                 "quant1d_kernel.cuh", "quant1d_sr.cu", "quant1d_sr_kernel.cuh", "quant2d.cu", "tile_pipeline.cuh",
-                 "tma.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
+                 "quant1d_common.cuh", "quant1d_kernel.cuh", "quant1d_sr.cu", "quant1d_sr_kernel.cuh", "quant2d.cu",
+                 "tile_pipeline.cuh", "tma.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
+    # the kernel that quantizes with SR on both copies, without 4/6, 2D or a
+    # rowwise transform (quant1d_sr_kernel)
+    "quantize_sr": ["api.cu", "tmap.cu", "quant1d_common.cuh", "quant1d_sr.cu", "quant1d_sr_kernel.cuh",
+                    "tile_pipeline.cuh", "tma.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
     "amax": ["api.cu", "amax.cu", "tile_pipeline.cuh", "nvfp4_device.cuh", "nvfp4_internal.h"],
 }
 
@@ -102,6 +106,12 @@ def source_hash(kernel: str = "quantize") -> str:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
+
+
+def sources_of(kernel: str, flags: int) -> str:
+    """The KERNEL_SOURCES key of the kernel that runs `kernel` with `flags`."""
+    sr_both = flags & 32 and flags & 1 and flags & 2 and not flags & (4 | 8 | 64)  # SR, R + C; no 2D, RHT_ROW, 4/6
+    return "quantize_sr" if kernel == "quantize" and sr_both else kernel
 
 
 def traffic_of(part: str, kernel: str):
@@ -228,7 +238,7 @@ def _kernel_roofline(part, kernel, flags, M, N, ms, hbm_peak, peak_kind, sms, sm
     rec["frac"] = round(rec["achieved"] / rec["peak"], 4)
     rec["peak_kind"] = peak_kind if rec["bound"] == "hbm" else "derived from the SM count, the measured " \
                                                                  "multiply rate and the maximum SM clock"
-    t = traffic_of(part, kernel)
+    t = traffic_of(part, sources_of(kernel, flags))
     rec["traffic"] = t
     if t is not None:
         rec["dram_gbs"] = round(t / (ms * 1e-3) / 1e9, 1)

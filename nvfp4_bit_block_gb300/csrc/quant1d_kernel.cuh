@@ -27,10 +27,7 @@
 // Sources: "Four Over Six (4/6)" technical summary (Problem statement,
 // Methodology, Implementation details) and "Pretraining Large Language Models
 // with NVFP4" sections 1, 2b and 2d.
-#include "nvfp4_device.cuh"
-#include "nvfp4_internal.h"
-#include "tile_pipeline.cuh"
-#include "tma.cuh"
+#include "quant1d_common.cuh"
 
 #ifndef NVFP4_Q1D_MIN_CTAS
 #define NVFP4_Q1D_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for
@@ -39,10 +36,7 @@
 namespace nvfp4 {
 namespace q1d {
 
-using tile::kTM;
-using tile::kTN;
 constexpr int kStashBytes = kTM * kTN * 4;  // Philox word 1 per element, 64 KB
-constexpr int kBlockThreads = 256;
 // Tile width (columns) of the 1D kernel: 64 x 128 tiles for plain
 // round-to-nearest, whose CTAs are bound by the latency of a tile's work (a
 // narrower tile halves it, and with it the cost of the launch's first and
@@ -60,23 +54,6 @@ constexpr int tile_width() { return (Q46 || SR || RHT != 0) ? kTN : kTN / 2; }
 __device__ __forceinline__ uint32_t stash_off(int r, int c) {
   const int q = c >> 2;
   return (uint32_t)r * 1024u + (uint32_t)((q ^ ((q >> 3) & 7) ^ ((r & 1) << 1)) << 4) + (uint32_t)(c & 3) * 4u;
-}
-
-// Per-copy scale constants: den = Q*alpha and its correctly rounded
-// reciprocal for Q = 6 and Q = 4, and the shared (d, 1/d) table of alpha.
-struct CopyScales {
-  float den6, rden6, den4, rden4;
-  const float2* tbl;
-};
-
-__device__ __forceinline__ CopyScales make_scales(float alpha, const float2* tbl) {
-  CopyScales c;
-  c.den6 = __fmul_rn(6.0f, alpha);
-  c.den4 = __fmul_rn(4.0f, alpha);
-  c.rden6 = (c.den6 != 0.0f) ? __frcp_rn(c.den6) : 0.0f;
-  c.rden4 = (c.den4 != 0.0f) ? __frcp_rn(c.den4) : 0.0f;
-  c.tbl = tbl;
-  return c;
 }
 
 // v = z * inv for 16 values (packed), then SR rounding or, for a max-4
@@ -177,27 +154,6 @@ __device__ __forceinline__ void quant_block16(const float* z, const CopyScales& 
   const bool four = s4 < s6;
   codes = four ? c4 : c6;
   e = four ? e4 : e6;
-}
-
-// a2 and the checks every 1D kernel makes first: alpha of each copy (block 0
-// writes both), the status of each produced copy's amax, and the 1 KB
-// alignment of the dynamic shared memory that the 128-byte swizzle needs.
-// False when the kernel must stop; block 0 has recorded why.
-__device__ __forceinline__ bool begin_tensor(const QuantArgs& a, bool row, bool col, float den, const uint8_t* smem,
-                                             float& alpha_r, float& alpha_c) {
-  const float A_r = a.amax[0], A_c = a.amax[1];
-  alpha_r = __fdiv_rn(A_r, den);
-  alpha_c = __fdiv_rn(A_c, den);
-  const int st_r = row ? amax_status(A_r) : 0;
-  const int st_c = col ? amax_status(A_c) : 0;
-  const bool misaligned = (tile::smem_u32(smem) & 1023u) != 0u;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    a.alpha[0] = alpha_r;
-    a.alpha[1] = alpha_c;
-    if ((st_r || st_c) && a.status) *a.status = st_r ? st_r : st_c;
-    if (misaligned && !(st_r || st_c) && a.status) *a.status = kStatusPipeline;
-  }
-  return !(st_r || st_c || misaligned);
 }
 
 // Scale bytes of a block with maximum b (e4 only with 4/6).

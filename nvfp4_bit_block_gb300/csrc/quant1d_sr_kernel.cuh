@@ -31,7 +31,7 @@
 // (4/6)" technical summary (Problem statement: E2M1 grid and block scaling).
 #include <type_traits>
 
-#include "quant1d_kernel.cuh"
+#include "quant1d_common.cuh"
 
 namespace nvfp4 {
 namespace q1d {

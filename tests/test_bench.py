@@ -49,6 +49,11 @@ def test_traffic_is_null_for_a_stale_capture(monkeypatch):
     assert bench.traffic_of("t", "quantize") is None
     monkeypatch.setattr(bench, "TRAFFIC", {("t", "quantize"): (123, bench.source_hash())})
     assert bench.traffic_of("t", "quantize") == 123
+    # SR on both copies without 4/6, 2D or a rowwise transform runs in its own kernel
+    assert bench.sources_of("quantize", 1 | 2 | 16 | 32) == "quantize_sr"
+    assert bench.sources_of("quantize", 1 | 2 | 32 | 64) == "quantize"
+    assert bench.sources_of("quantize", 1 | 32) == "quantize"
+    assert bench.sources_of("amax", 1 | 2 | 32) == "amax"
 
 
 def test_reference_arm_prints_one_contract_line():
