@@ -209,11 +209,11 @@ def test_swizzled_scales_are_the_plain_scales_relaid(flags):
 @pytest.mark.parametrize("flags,sel", [(ROW | COL, 0), (ROW | COL | F46, 1), (ROW | COL | RHT_COL | SR, 0),
                                        (ROW | F46 | SR, 2), (COL, 0)])
 def test_more_tiles_than_one_round(flags, sel):
-    """A 1984 x 4096 tensor has 496 tiles of 64 x 256: more than one round of
-    the persistent grid on 152 SMs at three or two CTAs per SM, and not a
-    multiple of either, so CTAs walk different numbers of tiles.  Every code
-    and scale byte equals the oracle's, and the tiled scale layout is the
-    plain one relaid."""
+    """A 1984 x 4096 tensor has 496 tiles of 64 x 256 (992 of 64 x 128 for
+    plain round-to-nearest): more than one round of the persistent grid on
+    152 SMs at two, three or four CTAs per SM, and not a multiple of any, so
+    CTAs walk different numbers of tiles.  Every code and scale byte equals
+    the oracle's, and the tiled scale layout is the plain one relaid."""
     M, N = 1984, 4096
     assert torch.cuda.get_device_properties(0).multi_processor_count * 3 < (M // 64) * (N // 256)
     bits = small_input(M, N, kind="grad" if flags & SR else "act")
