@@ -85,28 +85,27 @@ __device__ __forceinline__ void static_for(F& f) {
   }
 }
 
-// Write the staged rowwise codes of one tile: thread t writes bytes
-// 32 (t % 4) .. +31 of tile row t / 4 (the row's valid bytes are cols / 2).
+// Write the staged rowwise codes of one tile: thread t writes 16-byte chunk
+// t % 8 of tile rows t / 8 and t / 8 + 32 (a row's valid bytes are cols / 2).
+// A quarter warp reads one whole 128-byte row, so the reads are free of bank
+// conflicts, and a warp's stores cover four whole rows.
 __device__ __forceinline__ void write_row_outputs(const uint8_t* rstage, uint8_t* q_row, int64_t hN,
                                                   const tile::Coord& tc, int rows, int cols, int tid) {
-  const int r = tid >> 2, j = tid & 3;
-  const int nb = cols / 2 - 32 * j;  // a multiple of 8
-  if (r >= rows || nb <= 0) return;
-  const uint4 lo = *reinterpret_cast<const uint4*>(rstage + r * 128 + 32 * j);
-  const uint4 hi = *reinterpret_cast<const uint4*>(rstage + r * 128 + 32 * j + 16);
-  uint8_t* dst = q_row + (tc.R0 + r) * hN + tc.C0 / 2 + 32 * j;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(dst);
-  if (nb >= 32 && (addr & 31) == 0) {
-    tile::st_v8(dst, make_uint2(lo.x, lo.y), make_uint2(lo.z, lo.w), make_uint2(hi.x, hi.y), make_uint2(hi.z, hi.w));
-  } else if (nb >= 32 && (addr & 15) == 0) {
-    *reinterpret_cast<uint4*>(dst) = lo;
-    *reinterpret_cast<uint4*>(dst + 16) = hi;
-  } else {
-    const uint2 p[4] = {make_uint2(lo.x, lo.y), make_uint2(lo.z, lo.w), make_uint2(hi.x, hi.y),
-                        make_uint2(hi.z, hi.w)};
+  const int c = tid & 7;
+  if (16 * c >= cols / 2) return;  // cols / 2 is a multiple of 8; chunks are whole or absent
+  const bool half = 16 * c + 8 >= cols / 2;  // only the chunk's first 8 bytes are in the tensor
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (8 * k < nb) *reinterpret_cast<uint2*>(dst + 8 * k) = p[k];
+  for (int h = 0; h < 2; ++h) {
+    const int r = (tid >> 3) + 32 * h;
+    if (r >= rows) break;
+    const uint4 v = *reinterpret_cast<const uint4*>(rstage + r * 128 + 16 * c);
+    uint8_t* dst = q_row + (tc.R0 + r) * hN + tc.C0 / 2 + 16 * c;
+    if (!half && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+      *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(v.x, v.y);
+      if (!half) *reinterpret_cast<uint2*>(dst + 8) = make_uint2(v.z, v.w);
+    }
   }
 }
 
@@ -121,10 +120,12 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   uint8_t* sstage = cstage + tile::kCStageBytes;                 // 1 KB
   uint8_t* rstage = sstage + tile::kSStageBytes;                 // 8 KB
   float* rinv = reinterpret_cast<float*>(rstage + kRStageBytes);  // 4.5 KB
-  float2* tbl = reinterpret_cast<float2*>(rinv + kRInvBytes / 4);  // 2 x 128 (d, 1/d)
-  // entry 127 of each table is free (scale bytes never exceed 0x7E): the
-  // tile barriers of buffer 0 and buffer 1
-  const uint32_t bar0 = tile::smem_u32(tbl + 127), bar1 = tile::smem_u32(tbl + 255);
+  // 1/d per scale byte e: rowwise copy tinv[e], columnwise tinv[128 + e]
+  // (4-byte entries: lanes reading different bytes share a bank only when
+  // the bytes are 32 apart), then the two tile barriers
+  float* tinv = rinv + kRInvBytes / 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tinv + 256);
+  const uint32_t bar0 = tile::smem_u32(bars), bar1 = tile::smem_u32(bars + 1);
 
   float alpha_r, alpha_c;
   if (!begin_tensor(a, true, true, kAlphaDen, smem, alpha_r, alpha_c)) return;
@@ -151,11 +152,11 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       if (wn.valid()) issue(1, wn.coord());
     }
   }
-  if ((tid & 127) != 127) tbl[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r);
+  tinv[tid] = scale_entry(tid & 127, (tid >> 7) ? alpha_c : alpha_r).y;
   __syncthreads();  // barriers and tables ready
   if (!w.valid()) return;
-  const CopyScales scR = make_scales(alpha_r, tbl);
-  const CopyScales scC = make_scales(alpha_c, tbl + 128);
+  const CopyScales scR = make_scales(alpha_r, nullptr);  // den and 1/den; 1/d comes from tinv
+  const CopyScales scC = make_scales(alpha_c, nullptr);
   const uint32_t signs = RHT_COL ? rht_sign_bits(a.rht_k0, a.rht_k1) : 0u;
   const uint32_t k0 = a.sr_k0, k1 = a.sr_k1;
   const uint32_t N32 = (uint32_t)N;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
       wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
       const uint32_t e = scale_byte(block_absmax16(wd), scR.den6, scR.rden6);
-      rinv[(rq + 4 * k) * kRInvStride + rr] = scR.tbl[e].y;
+      rinv[(rq + 4 * k) * kRInvStride + rr] = tinv[e];
       st[st_step * k] = (uint8_t)e;
     }
   };
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       }
       const uint32_t ec0 = scale_byte(bm0, scC.den6, scC.rden6);
       const uint32_t ec1 = scale_byte(bm1, scC.den6, scC.rden6);
-      const float2 invc = make_float2(scC.tbl[ec0].y, scC.tbl[ec1].y);
+      const float2 invc = make_float2(tinv[128 + ec0], tinv[128 + ec1]);
       const float* ri = rinv + (p >> 3) * kRInvStride + 16 * rb;  // row i of the block: ri[i]
       uint8_t* rs = rstage + (16 * rb) * 128 + p;                  // row i: rs[128 * i]
       const uint64_t base = a.ctr_off + (uint64_t)((tc.R0 + 16 * rb) * N + tc.C0 + 2 * p);
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
 template <bool RHT_COL, bool NOCOPY = false>
 cudaError_t launch_sr_rc(const QuantArgs& a, cudaStream_t s) {
   constexpr int kSmem = 2 * tile::kTileBytes + tile::kCStageBytes + tile::kSStageBytes + kRStageBytes + kRInvBytes +
-                        256 * 8;
+                        256 * 4 + 2 * 8;
   auto kern = quant1d_sr_kernel<RHT_COL, NOCOPY>;
   static std::atomic<int> grid_cap[64] = {};
   int cap = 0;
