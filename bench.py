@@ -79,8 +79,8 @@ WIDE_PRODUCTS_PER_CLK_PER_SM = 32
 # (one pass; a cold single launch, so outputs still in L2 at its end are not
 # counted as written).
 TRAFFIC = {
-    ("linear_dy_16384x20480", "quantize_sr"): (689_220_000 + 362_040_000, "6960f11f7896163a"),
-    ("grad_rht_sr_16384x5120", "quantize_sr"): (167_860_000 + 56_610_000, "6960f11f7896163a"),
+    ("linear_dy_16384x20480", "quantize_sr"): (689_250_000 + 362_170_000, "561874a1ea1c2cb6"),
+    ("grad_rht_sr_16384x5120", "quantize_sr"): (167_877_888 + 56_236_544, "561874a1ea1c2cb6"),
 }
 CSRC = os.path.join(ROOT, "nvfp4_bit_block_gb300", "csrc")
 
