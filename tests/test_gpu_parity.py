@@ -121,8 +121,10 @@ def test_zero_and_empty_tensors():
 def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
     """An Inf or NaN anywhere makes the amax (plain, or of the Hadamard-
     transformed copy) non-finite; the quantize then reports NONFINITE and
-    writes nothing."""
-    for flags in (ROW | COL, ROW | COL | RHT_COL, ROW | COL | RHT_ROW | RHT_COL):
+    writes nothing (every kernel: the 1D round-to-nearest and 4/6 kernels,
+    the stochastic-rounding kernel of both copies, 2D)."""
+    for flags in (ROW | COL, ROW | COL | RHT_COL, ROW | COL | RHT_ROW | RHT_COL, ROW | COL | SR,
+                  ROW | COL | RHT_COL | SR, ROW | COL | F46, ROW | COL | TWO_D):
         for pattern, want in ((0x7F80, -6), (0xFFC0, -6)):
             bits = synthetic.weight(32, 32, 1)
             bits[5, 7] = pattern
@@ -136,7 +138,7 @@ def test_nonfinite_and_tiny_amax_report_a_status_and_write_nothing():
             torch.cuda.synchronize()
             assert out.status.item() == want
             assert not np.isfinite(amax.cpu().numpy()).any()
-            assert bool((out.q_row == 0xAB).all()) and bool((out.s_col == 0xAB).all())
+            assert all(bool((t == 0xAB).all()) for t in (out.q_row, out.s_row, out.q_col, out.s_col))
             st, am = oracle.amax(bits, flags)
             assert not np.isfinite(am).any()
             assert oracle.quantize(bits, 32, am, flags)["status"] == want
@@ -446,6 +448,24 @@ def test_counter_offset_reproduces_a_row_shard():
     assert np.array_equal(shard["q_row"], whole["q_row"][128:])
     assert np.array_equal(shard["q_col"], whole["q_col"][:, 64:])
     assert np.array_equal(shard["s_col"], whole["s_col"][:, 8:])
+
+
+@pytest.mark.parametrize("rht", [0, RHT_COL], ids=["plain", "rht_col"])
+def test_both_copies_with_sr_equal_the_single_copy_kernels(rht):
+    """With stochastic rounding on both copies, one Philox call per element
+    serves both (word 0 rowwise, word 1 columnwise; the one-pass kernel rounds
+    both in its columnwise pass).  Its rowwise copy equals what the
+    rowwise-only kernel makes, and its columnwise copy what the
+    columnwise-only kernel makes, from the same seeds and counters -- three
+    code paths of the library that share no rounding loop."""
+    bits = small_input(kind="grad")
+    x = to_device(bits)
+    kw = dict(sr_seed=0x77, rht_seed=0x99, counter_offset=(1 << 32) - 5000)
+    both = gpu_quantize(x, ROW | COL | SR | rht, 0, **kw)
+    row = gpu_quantize(x, ROW | SR, 0, **kw)
+    col = gpu_quantize(x, COL | SR | rht, 0, **kw)
+    assert np.array_equal(both["q_row"], row["q_row"]) and np.array_equal(both["s_row"], row["s_row"])
+    assert np.array_equal(both["q_col"], col["q_col"]) and np.array_equal(both["s_col"], col["s_col"])
 
 
 @pytest.mark.parametrize("offset", [(1 << 32) - 3000, (1 << 64) - 5000, (1 << 63) + 12345])
