@@ -112,3 +112,29 @@ def test_benchmark_line_on_the_gpu():
     assert d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 2 * 3  # amax and quantize per step
     assert d["clocks"]["sm_mhz"] is None or d["clocks"]["sm_mhz"] > 0
+
+
+def test_kernel_source_lists_cover_their_includes():
+    """A traffic capture is keyed by the hash of the sources its kernel is
+    built from: every local header that a listed translation unit includes,
+    directly or through another header, must be in the list too, or an edit
+    to it would leave a stale capture looking valid."""
+    import re
+    csrc = bench.CSRC
+    local = set(os.listdir(csrc))
+
+    def closure(name, seen):
+        if name in seen:
+            return
+        seen.add(name)
+        with open(os.path.join(csrc, name)) as f:
+            for inc in re.findall(r'#include\s+"([^"]+)"', f.read()):
+                if inc in local:
+                    closure(inc, seen)
+
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        need = set()
+        for name in files:
+            if name.endswith(".cu"):
+                closure(name, need)
+        assert need <= set(files), (kernel, sorted(need - set(files)))
